@@ -1,0 +1,345 @@
+/*
+ * CPU oracle for the Q2_K decode projections.  TEST INFRASTRUCTURE ONLY: the
+ * tests, the smoke check and the bench's CPU-baseline leg call it; the CUDA
+ * library never does, and the two share no code.
+ *
+ * Plain, slow, obviously correct C.  Floating point is fp64 unless the
+ * method fixes a precision (the q8_1 encoding decides integers in fp32, and
+ * the dequantised rows are bf16 by definition).
+ *
+ * Sources (the metrale docs pages):
+ *  - engram_v41.rs, `ENGRAM_ROW_BYTES` and the `wkv_q2k` field doc: one Q2_K
+ *    super-block is 84 bytes and holds 256 weights; a weight matrix is
+ *    `[out, in/256]` blocks, row-major, as GGUF ships it; `y = x W^T`.
+ *  - engram_v41.rs, `rows_from_q2k`: rows are dequantised to bf16, one block
+ *    per 256-wide row, in `[token][col]` order.
+ *  - attn_v41/decode.rs, `q_kv_projections`: one q8_1 quantisation feeds
+ *    both the `wq_a` and `wkv` projections (m <= 8).
+ *  - moe_v41/init.rs, `MoeV41::new`: gate and up run as one expert batch,
+ *    SwiGLU is fused with the q8_1 requantisation of `h`, and the expert
+ *    outputs are accumulated with the route weights.
+ *
+ * Readings taken where the pages are silent (each listed in the design
+ * notes):
+ *  - Q2_K byte order: scales[16] | qs[64] | d (fp16 LE) | dmin (fp16 LE).
+ *    Weight p in [0,256) lies in sub-block j = p/16; scales[j] low nibble is
+ *    the scale, high nibble the min; its 2-bit code is bits
+ *    2*((p%128)/32) .. +1 of qs[32*(p/128) + p%32];
+ *    w_p = d*(scales[j]&15)*q_p - dmin*(scales[j]>>4).
+ *  - q8_1 block (36 bytes, 32 values): fp16 d, fp16 s, int8 q[32];
+ *    d32 = amax/127 (fp32 divide), q = round-half-away(x/d32) (fp32 divide,
+ *    0 when amax == 0), d = fp16_rn(d32), s = fp16_rn(f32(d) * sum(q)).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#define Q2K_BYTES 84
+#define Q2K_WEIGHTS 256
+#define Q8_1_BYTES 36
+#define Q8_1_VALUES 32
+
+/* ---- scalar formats ------------------------------------------------------ */
+
+/* IEEE binary16 bits -> exact double. */
+double oracle_fp16_to_double(uint16_t h)
+{
+    int sign = h >> 15;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+/* bf16 bits -> exact double. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* Finite float -> binary16 bits, round to nearest, ties to even. */
+uint16_t oracle_f32_to_fp16(float x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs((double)x);
+    if (isnan(x))
+        return 0x7E00;
+    if (a >= 65520.0) /* halfway between 65504 and 2^16 rounds to even -> inf */
+        return sign | 0x7C00;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: quantum 2^-24; n == 1024 is the smallest normal */
+        double n = nearbyint(a * ldexp(1.0, 24));
+        return sign | (uint16_t)n;
+    }
+    int ex;
+    frexp(a, &ex); /* a = fr * 2^ex, fr in [0.5, 1) */
+    int e = ex - 1; /* a in [2^e, 2^(e+1)) */
+    double n = nearbyint(ldexp(a, 10 - e)); /* 11-bit significand */
+    if (n == 2048.0) {
+        n = 1024.0;
+        e += 1;
+    }
+    if (e + 15 >= 31)
+        return sign | 0x7C00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)n - 1024));
+}
+
+/* Finite float -> bf16 bits, round to nearest, ties to even. */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if (isnan(x))
+        return (uint16_t)((u >> 16) | 0x40);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000);
+    double a = fabs((double)x);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    if (e < -126)
+        e = -126; /* bf16 subnormals share fp32's exponent floor */
+    double q = ldexp(1.0, e - 7); /* 8-bit significand quantum */
+    double n = nearbyint(a / q);
+    double r = n * q;
+    if (r >= ldexp(1.0, 128))
+        return sign | 0x7F80;
+    float rf = (float)r; /* exact: r is a bf16 value */
+    uint32_t ru;
+    memcpy(&ru, &rf, 4);
+    return sign | (uint16_t)(ru >> 16);
+}
+
+/* Round hi+lo (an exact value split as a double-double, |lo| <= ulp(hi)/2)
+ * to the nearest float, ties to even, without double rounding. */
+static float round_dd_to_f32(double hi, double lo)
+{
+    float f = (float)hi;
+    double back = (double)f;
+    if (back == hi || lo == 0.0)
+        return f;
+    /* The only double-rounding hazard: hi sits exactly half-way between two
+     * floats; then the sign of lo decides. */
+    float up = nextafterf(f, INFINITY), dn = nextafterf(f, -INFINITY);
+    double mid_up = ((double)f + (double)up) * 0.5;
+    double mid_dn = ((double)f + (double)dn) * 0.5;
+    if (hi == mid_up && lo < 0)
+        return f;
+    if (hi == mid_up && lo > 0)
+        return up;
+    if (hi == mid_dn && lo > 0)
+        return f;
+    if (hi == mid_dn && lo < 0)
+        return dn;
+    return f;
+}
+
+/* ---- Q2_K ----------------------------------------------------------------- */
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* 2-bit code of weight p in a block. */
+static int q2k_code(const uint8_t* blk, int p)
+{
+    const uint8_t* qs = blk + 16;
+    int byte = qs[32 * (p / 128) + (p % 32)];
+    int shift = 2 * ((p % 128) / 32);
+    return (byte >> shift) & 3;
+}
+
+/* Exact decoded weights of one 84-byte block (fp64; exact for every fp16
+ * d/dmin whose products span at most 53 bits, which holds for any block
+ * whose d and dmin lie within 2^33 of each other). */
+void oracle_q2k_decode_block(const uint8_t* blk, double* w)
+{
+    double d = oracle_fp16_to_double(rd16(blk + 80));
+    double dmin = oracle_fp16_to_double(rd16(blk + 82));
+    for (int p = 0; p < Q2K_WEIGHTS; ++p) {
+        int sc = blk[p / 16];
+        w[p] = d * (double)(sc & 15) * (double)q2k_code(blk, p) - dmin * (double)(sc >> 4);
+    }
+}
+
+/* bf16 bits of every weight of one block: the exact value rounded once to
+ * fp32 and then to bf16. */
+void oracle_q2k_decode_block_bf16(const uint8_t* blk, uint16_t* out)
+{
+    double d = oracle_fp16_to_double(rd16(blk + 80));
+    double dmin = oracle_fp16_to_double(rd16(blk + 82));
+    for (int p = 0; p < Q2K_WEIGHTS; ++p) {
+        int sc = blk[p / 16];
+        double a = d * (double)(sc & 15) * (double)q2k_code(blk, p); /* exact */
+        double b = dmin * (double)(sc >> 4);                          /* exact */
+        double s = a - b;
+        double bb = s - a; /* TwoSum of a and -b */
+        double err = (a - (s - bb)) + (-b - bb);
+        out[p] = oracle_f32_to_bf16(round_dd_to_f32(s, err));
+    }
+}
+
+/* Gather + dequantise: out[r, :] = bf16(decode(table row ids[r])), each row
+ * K/256 blocks.  ids == NULL means rows 0..n_rows-1.  An id outside
+ * [0, n_table_rows) yields a zero row; returns how many ids were bad. */
+int64_t oracle_q2k_dequant_rows(const uint8_t* table, int64_t n_table_rows, int64_t K,
+                                const int32_t* ids, int64_t n_rows, uint16_t* out)
+{
+    int64_t nb = K / Q2K_WEIGHTS, bad = 0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t src = ids ? (int64_t)ids[r] : r;
+        uint16_t* o = out + r * K;
+        if (src < 0 || src >= n_table_rows) {
+            memset(o, 0, (size_t)K * 2);
+            ++bad;
+            continue;
+        }
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_q2k_decode_block_bf16(table + (src * nb + b) * Q2K_BYTES, o + b * Q2K_WEIGHTS);
+    }
+    return bad;
+}
+
+/* Exact decoded matrix [N, K] (fp64). */
+void oracle_q2k_decode_matrix(const uint8_t* W, int64_t N, int64_t K, double* out)
+{
+    int64_t nb = K / Q2K_WEIGHTS;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_q2k_decode_block(W + (n * nb + b) * Q2K_BYTES, out + n * K + b * Q2K_WEIGHTS);
+}
+
+/* y[t, n] = sum_k w[n, k] * x[t, k]; W Q2_K [N, K], x fp64 [m, K],
+ * y fp64 [m, N].  Naive, fp64 accumulation in k order. */
+void oracle_q2k_matvec(const uint8_t* W, int64_t N, int64_t K, const double* x, int64_t m,
+                       double* y)
+{
+    int64_t nb = K / Q2K_WEIGHTS;
+    double w[Q2K_WEIGHTS];
+    for (int64_t t = 0; t < m; ++t)
+        for (int64_t n = 0; n < N; ++n)
+            y[t * N + n] = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < nb; ++b) {
+            oracle_q2k_decode_block(W + (n * nb + b) * Q2K_BYTES, w);
+            for (int64_t t = 0; t < m; ++t) {
+                double acc = 0.0;
+                const double* xr = x + t * K + b * Q2K_WEIGHTS;
+                for (int p = 0; p < Q2K_WEIGHTS; ++p)
+                    acc += w[p] * xr[p];
+                y[t * N + n] += acc;
+            }
+        }
+    }
+}
+
+/* ---- q8_1 ----------------------------------------------------------------- */
+
+/* bf16 x [m, K] with row stride ldx (elements) -> q8_1 rows, K/32 blocks of
+ * 36 bytes per row, rows contiguous. */
+void oracle_q8_1_quantize_rows(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, uint8_t* out)
+{
+    int64_t nblk = K / Q8_1_VALUES;
+    for (int64_t t = 0; t < m; ++t) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            float v[Q8_1_VALUES];
+            float amax = 0.0f;
+            for (int i = 0; i < Q8_1_VALUES; ++i) {
+                v[i] = (float)oracle_bf16_to_double(x[t * ldx + b * Q8_1_VALUES + i]);
+                float a = fabsf(v[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            volatile float d32 = amax / 127.0f; /* IEEE fp32 divide */
+            int8_t q[Q8_1_VALUES];
+            int sumq = 0;
+            for (int i = 0; i < Q8_1_VALUES; ++i) {
+                int qi = 0;
+                if (amax != 0.0f) {
+                    volatile float r = v[i] / d32; /* IEEE fp32 divide */
+                    qi = (int)roundf(r);           /* half away from zero */
+                }
+                q[i] = (int8_t)qi;
+                sumq += qi;
+            }
+            uint16_t dh = oracle_f32_to_fp16(d32);
+            float df = (float)oracle_fp16_to_double(dh);
+            volatile float sf = df * (float)sumq; /* fp32 multiply */
+            uint16_t sh = oracle_f32_to_fp16(sf);
+            uint8_t* o = out + (t * nblk + b) * Q8_1_BYTES;
+            o[0] = (uint8_t)(dh & 0xFF);
+            o[1] = (uint8_t)(dh >> 8);
+            o[2] = (uint8_t)(sh & 0xFF);
+            o[3] = (uint8_t)(sh >> 8);
+            memcpy(o + 4, q, Q8_1_VALUES);
+        }
+    }
+}
+
+/* q8_1 rows -> the values they stand for, f32(d) * q, exact in fp64. */
+void oracle_q8_1_dequant_rows(const uint8_t* xq, int64_t m, int64_t K, double* x)
+{
+    int64_t nblk = K / Q8_1_VALUES;
+    for (int64_t t = 0; t < m; ++t)
+        for (int64_t b = 0; b < nblk; ++b) {
+            const uint8_t* blk = xq + (t * nblk + b) * Q8_1_BYTES;
+            double d = oracle_fp16_to_double(rd16(blk));
+            for (int i = 0; i < Q8_1_VALUES; ++i)
+                x[t * K + b * Q8_1_VALUES + i] = d * (double)(int8_t)blk[4 + i];
+        }
+}
+
+/* ---- dense and elementwise ------------------------------------------------ */
+
+/* y[t, n] = sum_k x[t, k] * W[n, k], bf16 inputs, fp64 accumulation. */
+void oracle_dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx,
+                            const uint16_t* W, int64_t N, double* y)
+{
+    for (int64_t t = 0; t < m; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += oracle_bf16_to_double(x[t * ldx + k]) * oracle_bf16_to_double(W[n * K + k]);
+            y[t * N + n] = acc;
+        }
+}
+
+/* silu(z) = z / (1 + e^-z), fp64. */
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* h[i] = silu(g[i]) * u[i] over n values, fp64. */
+void oracle_swiglu(const double* g, const double* u, int64_t n, double* h)
+{
+    for (int64_t i = 0; i < n; ++i)
+        h[i] = oracle_silu(g[i]) * u[i];
+}
+
+/* y[n] = sum_e w[e] * v[e, n] over E rows of length N, in e order, fp64. */
+void oracle_weighted_sum(const double* v, const float* w, int64_t E, int64_t N, double* y)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0;
+        for (int64_t e = 0; e < E; ++e)
+            acc += (double)w[e] * v[e * N + n];
+        y[n] = acc;
+    }
+}
+
+/* fp64 values -> bf16 bits (fp64 -> fp32 -> bf16, each round to nearest). */
+void oracle_round_bf16(const double* v, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f32_to_bf16((float)v[i]);
+}
+
+int oracle_block_bytes(void) { return Q2K_BYTES; }
+int oracle_q8_1_block_bytes(void) { return Q8_1_BYTES; }

@@ -1,0 +1,372 @@
+"""Pins for the CPU oracle: each check compares it with something other than
+itself -- the pages' stated facts, library routines (NumPy / SciPy), exact
+rational arithmetic, closed forms and invariants -- so that a dropped term,
+a wrong sign, index or nibble, or a transposed operand fails one of them.
+
+The Q2_K bit order inside ``qs`` is a reading of the GGUF Q2_K format (the
+pages give only the 84-byte size, the field list and the formula); the
+bijectivity and one-hot checks below pin its internal consistency, not its
+agreement with a real GGUF file (parity unpinned there).
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def page_facts():
+    facts = {}
+    with open(os.path.join(GOLDEN, "page_facts.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = (s.strip() for s in line.split("="))
+                facts[k] = int(v)
+    return facts
+
+
+def make_block(scales, qs, d, dmin):
+    b = np.zeros(84, dtype=np.uint8)
+    b[0:16] = np.asarray(scales, dtype=np.uint8)
+    b[16:80] = np.asarray(qs, dtype=np.uint8)
+    b[80:84] = np.array([d, dmin], dtype=np.float16).view(np.uint8)
+    return b
+
+
+# ---- exact rational reference roundings (independent of the oracle's C) ----
+
+def frac_round_even(x: Fraction) -> int:
+    fl = math.floor(x)
+    r = x - fl
+    if r > Fraction(1, 2):
+        return fl + 1
+    if r < Fraction(1, 2):
+        return fl
+    return fl if fl % 2 == 0 else fl + 1
+
+
+def frac_to_binary(x: Fraction, sig_bits: int, emin: int):
+    """Nearest value with ``sig_bits`` significand bits (ties to even),
+    exponent floor ``emin`` (subnormals below), no overflow handling."""
+    if x == 0:
+        return Fraction(0)
+    s = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    q = Fraction(2) ** (e - (sig_bits - 1))
+    return s * frac_round_even(a / q) * q
+
+
+def bf16_bits_of(v: Fraction) -> int:
+    f = np.float32(float(v))  # v is a bf16 value: exact in fp32
+    return int(np.array([f], dtype=np.float32).view(np.uint32)[0] >> 16)
+
+
+# ---- the pages' stated facts -------------------------------------------------
+
+def test_block_size_is_the_pages_84_bytes():
+    facts = page_facts()
+    assert oracle.block_bytes() == facts["q2k_block_bytes"] == 84
+    assert 16 + 64 + 2 + 2 == facts["q2k_block_bytes"]
+    assert facts["q2k_block_weights"] == oracle.Q2K_WEIGHTS
+    # "84 bytes per 256 weights, against 512 in bf16"
+    assert facts["bf16_bytes_per_256"] == 2 * facts["q2k_block_weights"]
+    assert oracle.Q8_1_BYTES == 2 + 2 + 32
+
+
+# ---- scalar formats ----------------------------------------------------------
+
+def test_fp16_decode_matches_numpy_for_every_finite_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    got = np.array([oracle.fp16_to_double(int(b)) for b in bits[finite]])
+    np.testing.assert_array_equal(got, ref[finite])
+
+
+def test_f32_to_fp16_matches_numpy_round_to_nearest_even():
+    g = np.random.default_rng(1)
+    vals = np.concatenate([
+        g.standard_normal(4000).astype(np.float32) * np.float32(10.0) ** g.integers(-9, 5, 4000),
+        np.float32(2.0) ** g.integers(-26, 16, 500).astype(np.float32),
+        # exact half-way cases between consecutive fp16 values
+        (np.arange(1000, 1200, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -10),
+        (np.arange(0, 300, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -24),
+        np.array([65504.0, 65519.0, 65520.0, 0.0, -0.0, 6.1e-5, -5.9e-8], dtype=np.float32),
+    ])
+    vals = vals[np.abs(vals) < np.float32(65520.0)]  # overflow to inf is checked apart
+    assert oracle.f32_to_fp16(65520.0) == 0x7C00 and oracle.f32_to_fp16(-1e6) == 0xFC00
+    got = np.array([oracle.f32_to_fp16(float(v)) for v in vals], dtype=np.uint16)
+    ref = vals.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_f32_to_bf16_is_the_nearest_even_by_exact_arithmetic():
+    g = np.random.default_rng(2)
+    u = g.integers(0, 2 ** 32, 3000, dtype=np.uint64).astype(np.uint32)
+    vals = u.view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) < np.float32(3e38))]
+    ties = (np.arange(200, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    vals = np.concatenate([vals, ties[np.isfinite(ties)], np.float32([1e-40, -3e-45, 0.0])])
+    for v in vals:
+        ref = bf16_bits_of(frac_to_binary(Fraction(float(v)), 8, -126))
+        got = oracle.f32_to_bf16(float(v))
+        sign = 0x8000 if np.signbit(v) else 0
+        assert got == (ref | sign), (float(v), hex(got), hex(ref))
+
+
+# ---- Q2_K decode -------------------------------------------------------------
+
+def test_all_codes_three_gives_closed_form_per_subblock():
+    # Every 2-bit code = 3, so the layout of qs does not matter; sub-block j
+    # (16 consecutive weights) uses scales[j]: low nibble scale, high min.
+    sc = np.arange(16) % 16
+    mn = (15 - np.arange(16)) % 16
+    d, dmin = 0.5, 0.125
+    blk = make_block((mn << 4) | sc, np.full(64, 0xFF), d, dmin)
+    w = oracle.decode_block(blk)
+    p = np.arange(256)
+    np.testing.assert_array_equal(w, 3 * d * sc[p // 16] - dmin * mn[p // 16])
+
+
+def test_all_codes_zero_gives_minus_min():
+    sc = np.full(16, 7)
+    mn = np.arange(16)
+    blk = make_block((mn << 4) | sc, np.zeros(64), 2.0, 0.25)
+    w = oracle.decode_block(blk)
+    np.testing.assert_array_equal(w, -0.25 * np.repeat(mn, 16))
+
+
+def test_d_and_dmin_fields_are_not_swapped():
+    blk = make_block(np.full(16, (1 << 4) | 1), np.full(64, 0x55), 4.0, 1.0)  # codes 1
+    assert np.all(oracle.decode_block(blk) == 4.0 * 1 * 1 - 1.0 * 1)
+
+
+def test_each_qs_bit_drives_exactly_one_weight_and_all_256_are_covered():
+    low, high = [], []
+    for byte in range(64):
+        for bit in range(8):
+            qs = np.zeros(64, dtype=np.uint8)
+            qs[byte] = 1 << bit
+            w = oracle.decode_block(make_block(np.full(16, 1), qs, 1.0, 0.0))
+            nz = np.flatnonzero(w)
+            assert len(nz) == 1
+            val = w[nz[0]]
+            assert val == (1.0 if bit % 2 == 0 else 2.0)
+            (low if bit % 2 == 0 else high).append(int(nz[0]))
+            # the low and high bit of one code land on the same weight
+            if bit % 2 == 1:
+                assert high[-1] == low[-1]
+    assert sorted(low) == list(range(256))
+    assert sorted(high) == list(range(256))
+
+
+def test_one_hot_code_reading():
+    # Reading of the GGUF layout: weight p takes bits 2*((p%128)//32) of
+    # qs[32*(p//128) + p%32].  A one-hot code decodes to the unit vector.
+    for p in range(256):
+        qs = np.zeros(64, dtype=np.uint8)
+        qs[32 * (p // 128) + p % 32] = 1 << (2 * ((p % 128) // 32))
+        w = oracle.decode_block(make_block(np.full(16, 1), qs, 1.0, 0.0))
+        e = np.zeros(256)
+        e[p] = 1.0
+        np.testing.assert_array_equal(w, e)
+
+
+def test_scale_byte_affects_sixteen_consecutive_weights():
+    base = synth.q2k_blocks(0, "pin.scales", 1)[0]
+    w0 = oracle.decode_block(base)
+    for j in range(16):
+        b = base.copy()
+        b[j] ^= 0x11
+        changed = np.flatnonzero(oracle.decode_block(b) != w0)
+        assert set(changed) <= set(range(16 * j, 16 * j + 16))
+        assert len(changed) > 0
+
+
+def test_decode_bf16_is_exact_value_rounded_once_to_f32_then_bf16():
+    blocks = synth.q2k_blocks(3, "pin.bf16", 6)
+    # add extreme d/dmin combinations (subnormal and large fp16)
+    extra = []
+    for d, dm in [(6.1e-5, 60000.0), (60000.0, 5.96e-8), (1e-7, 1e-7), (1000.0, 3.0)]:
+        b = blocks[0].copy()
+        b[80:84] = np.array([d, dm], dtype=np.float16).view(np.uint8)
+        extra.append(b)
+    for blk in list(blocks) + extra:
+        rows, bad = oracle.dequant_rows(blk, 1, 256, None, 1)
+        assert bad == 0
+        d = Fraction(float(blk[80:82].view(np.float16)[0]))
+        dm = Fraction(float(blk[82:84].view(np.float16)[0]))
+        w_exact = oracle.decode_block(blk)
+        for p in range(0, 256, 7):
+            j = p // 16
+            sc, mn = int(blk[j]) & 15, int(blk[j]) >> 4
+            byte = int(blk[16 + 32 * (p // 128) + p % 32])
+            q = (byte >> (2 * ((p % 128) // 32))) & 3
+            exact = d * sc * q - dm * mn
+            f32 = frac_to_binary(exact, 24, -126)
+            ref = bf16_bits_of(frac_to_binary(f32, 8, -126))
+            if exact < 0 and ref == 0:
+                ref = 0x8000
+            assert int(rows[0, p]) == ref, (p, float(exact))
+            # the fp64 decode is exact whenever the products span <= 53 bits
+            if abs(float(d)) > 0 and abs(float(dm)) > 0 and max(d, dm) / min(d, dm) < 2 ** 30:
+                assert Fraction(w_exact[p]) == exact
+
+
+def test_dequant_rows_gather_equals_contiguous_copy_and_flags_bad_ids():
+    K = 512
+    table = synth.q2k_matrix(4, "pin.table", 10, K)
+    ids = np.array([3, 3, 0, 9, 5], dtype=np.int32)
+    got, bad = oracle.dequant_rows(table, 10, K, ids, len(ids))
+    assert bad == 0
+    ref, _ = oracle.dequant_rows(np.ascontiguousarray(table[ids]), len(ids), K, None, len(ids))
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(got[0], got[1])
+    got2, bad2 = oracle.dequant_rows(table, 10, K, np.array([1, -1, 10, 2], np.int32), 4)
+    assert bad2 == 2
+    assert not got2[1].any() and not got2[2].any()
+    row1, _ = oracle.dequant_rows(table, 10, K, np.array([1], np.int32), 1)
+    np.testing.assert_array_equal(got2[0], row1[0])
+
+
+# ---- q8_1 --------------------------------------------------------------------
+
+def q8_fields(xq, m, K):
+    blk = xq.reshape(m, K // 32, 36)
+    d = blk[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float32)
+    s = blk[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float32)
+    q = blk[..., 4:].view(np.int8).astype(np.int32)
+    return d, s, q
+
+
+def test_q8_1_invariants_on_random_rows():
+    m, K = 3, 1024
+    x = synth.bf16_normal(5, "pin.q8", (m, K))
+    xq = oracle.q8_1_quantize(x)
+    d, s, q = q8_fields(xq, m, K)
+    xv = synth.bf16_bits_to_f32(x).reshape(m, K // 32, 32)
+    amax = np.abs(xv).max(axis=-1)
+    d32 = (amax / np.float32(127.0)).astype(np.float32)
+    assert np.all(np.abs(q) <= 127)
+    assert np.all(np.abs(q).max(axis=-1) == 127)
+    # |x - d32 q| <= d32/2, up to the one fp32 rounding of x/d32 (half an
+    # ulp of a value below 128, i.e. 2^-17)
+    err = np.abs(xv.astype(np.float64) - d32[..., None].astype(np.float64) * q)
+    assert np.all(err <= d32[..., None].astype(np.float64) * (0.5 + 2.0 ** -17))
+    # stored d is fp16(d32) (NumPy's round-to-nearest-even cast)
+    np.testing.assert_array_equal(d, d32.astype(np.float16).astype(np.float32))
+    # s = fp16(f32(d) * sum q)
+    sref = (d * q.sum(axis=-1).astype(np.float32)).astype(np.float32).astype(np.float16).astype(np.float32)
+    np.testing.assert_array_equal(s, sref)
+
+
+def test_q8_1_rounds_half_away_from_zero_and_zero_block():
+    vals = np.zeros(64, dtype=np.float32)
+    vals[:8] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5]
+    x = synth.f32_to_bf16_bits(vals)[None, :]
+    d, s, q = q8_fields(oracle.q8_1_quantize(x), 1, 64)
+    assert d[0, 0] == 1.0
+    assert list(q[0, 0, :8]) == [127, 3, -3, 1, -1, 2, -2, 127]
+    assert d[0, 1] == 0.0 and s[0, 1] == 0.0 and not q[0, 1].any()
+
+
+def test_q8_1_power_of_two_scaling_is_exact():
+    x = synth.bf16_normal(6, "pin.q8s", (2, 256))
+    x2 = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x) * np.float32(2.0))
+    d1, _, q1 = q8_fields(oracle.q8_1_quantize(x), 2, 256)
+    d2, _, q2 = q8_fields(oracle.q8_1_quantize(x2), 2, 256)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(d2, 2 * d1)
+
+
+def test_q8_1_dequant_is_d_times_q():
+    x = synth.bf16_normal(7, "pin.q8d", (2, 128))
+    xq = oracle.q8_1_quantize(x)
+    d, _, q = q8_fields(xq, 2, 128)
+    np.testing.assert_array_equal(oracle.q8_1_dequant(xq, 2, 128),
+                                  (d[..., None].astype(np.float64) * q).reshape(2, 128))
+
+
+# ---- projections -----------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,m", [(1, 256, 1), (3, 512, 2), (5, 256, 8), (4, 768, 3)])
+def test_matvec_equals_numpy_matmul_of_decoded_matrix(N, K, m):
+    W = synth.q2k_matrix(8, f"pin.mv{N}x{K}", N, K)
+    x = synth.bf16_bits_to_f32(synth.bf16_normal(8, f"pin.mvx{m}", (m, K))).astype(np.float64)
+    Wd = oracle.decode_matrix(W, N, K)
+    np.testing.assert_allclose(oracle.matvec(W, N, K, x), x @ Wd.T, rtol=1e-12, atol=1e-12)
+
+
+def test_matvec_unit_vector_selects_one_column_exactly():
+    N, K = 5, 512
+    W = synth.q2k_matrix(9, "pin.col", N, K)
+    Wd = oracle.decode_matrix(W, N, K)
+    for k in (0, 1, 17, 255, 256, 300, 511):
+        x = np.zeros((1, K))
+        x[0, k] = 1.0
+        np.testing.assert_array_equal(oracle.matvec(W, N, K, x)[0], Wd[:, k])
+
+
+def test_matvec_rows_are_independent_blocks():
+    # a row's output depends only on its own blocks: permuting rows of W
+    # permutes y.
+    N, K = 4, 512
+    W = synth.q2k_matrix(10, "pin.perm", N, K)
+    x = np.random.default_rng(0).standard_normal((2, K))
+    perm = [2, 0, 3, 1]
+    np.testing.assert_array_equal(oracle.matvec(W[perm], N, K, x), oracle.matvec(W, N, K, x)[:, perm])
+
+
+def test_dense_gemm_matches_numpy_matmul():
+    x = synth.bf16_normal(11, "pin.gx", (3, 96))
+    W = synth.bf16_normal(11, "pin.gw", (7, 96), std=0.02)
+    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ synth.bf16_bits_to_f32(W).astype(np.float64).T
+    np.testing.assert_allclose(oracle.dense_gemm(x, W), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_silu_matches_scipy_and_odd_identity():
+    from scipy.special import expit
+    z = np.linspace(-30, 30, 601)
+    got = np.array([oracle.silu(v) for v in z])
+    np.testing.assert_allclose(got, z * expit(z), rtol=1e-14, atol=1e-300)
+    # silu(z) - silu(-z) = z
+    np.testing.assert_allclose(got - got[::-1], z, atol=1e-12)
+    assert oracle.silu(0.0) == 0.0
+
+
+def test_weighted_sum_matches_numpy_and_one_hot_selects():
+    v = np.random.default_rng(1).standard_normal((4, 9))
+    w = np.array([0.1, 0.2, 0.3, 0.4], dtype=np.float32)
+    np.testing.assert_allclose(oracle.weighted_sum(v, w), w.astype(np.float64) @ v, rtol=1e-14)
+    np.testing.assert_array_equal(oracle.weighted_sum(v, np.float32([0, 0, 1, 0])), v[2])
+
+
+def test_moe_chain_single_expert_and_quantised_agreement():
+    dim, inter = 256, 256
+    gate = [synth.q2k_matrix(12, f"pin.g{e}", inter, dim) for e in range(2)]
+    up = [synth.q2k_matrix(12, f"pin.u{e}", inter, dim) for e in range(2)]
+    down = [synth.q2k_matrix(12, f"pin.d{e}", dim, inter) for e in range(2)]
+    x = synth.bf16_normal(12, "pin.x", (1, dim))
+    both = oracle.moe_m1(x, gate, up, down, np.float32([1.0, 0.0]), dim, inter)
+    one = oracle.moe_m1(x, gate[:1], up[:1], down[:1], np.float32([1.0]), dim, inter)
+    np.testing.assert_array_equal(both["y"], one["y"])
+    # swapping expert order together with the weights leaves y unchanged
+    w = np.float32([0.3, 0.7])
+    a = oracle.moe_m1(x, gate, up, down, w, dim, inter)["y"]
+    b = oracle.moe_m1(x, gate[::-1], up[::-1], down[::-1], w[::-1], dim, inter)["y"]
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+    q = oracle.moe_m1(x, gate, up, down, w, dim, inter, quantized=True)["y"]
+    assert np.max(np.abs(q - a)) / np.linalg.norm(a) < 1e-2
