@@ -1,0 +1,534 @@
+#!/usr/bin/env python
+"""Benchmark of the Q2_K decode projection on GB300.
+
+Headline workload: the m=1 Q2_K GEMV with bf16 activations at
+N = K = 16384 (88,080,384 weight bytes), one C-ABI call per step.  The
+metric is weight-stream GB/s (and us per call); the roofline fraction is
+against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+
+* Steps are timed in CUDA graphs of up to 100 C-ABI calls, with CUDA events
+  on the launching stream, bracketed by a barrier and synchronize.
+* L2 is defeated by cycling R weight copies with R x bytes >= 3 x L2.
+* Clocks and throttle reasons are sampled with nvidia-smi during the timed
+  region.
+* e2e repeats the metric with host buffers: each step copies the weights
+  and x from pinned host memory, calls the C ABI, and reads y back.
+* cpu_baseline times the CPU oracle (one thread) on a bounded sample.
+* --impl reference times the CPU oracle on the same workload (rank 0 only).
+* --all also times every configuration of the sweep and prints one JSON
+  object per configuration to stderr (and to gpurun_out/bench_all.jsonl when
+  that folder exists).
+With torchrun (N > 1) every rank runs an independent replica (the path is
+replicated, not sharded); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+BASELINE = json.load(open(os.path.join(ROOT, "BASELINE.json")))
+METRIC = BASELINE["metric"]
+N_HEAD = K_HEAD = 16384
+W_BYTES_HEAD = N_HEAD * (K_HEAD // 256) * 84
+ALG_BYTES_HEAD = W_BYTES_HEAD + 2 * K_HEAD + 4 * N_HEAD  # weights + bf16 x + fp32 y
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1931.4)), "measured"
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("q2k_mv.cu", "q2k_common.cuh"):
+        h.update(open(os.path.join(ROOT, "mmvq_q2_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the headline kernel from the committed ncu
+    summary, or None when the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---- distributed plumbing (host logic, covered by gloo tests) --------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(elapsed_s: float, units: float, group=None):
+    """(max elapsed over ranks, sum of units over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---- clocks -------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---- timing helpers -----------------------------------------------------------------
+
+def graph_time(launch, steps: int, warmup: int, batch: int = 100):
+    """Time exactly `steps` calls of launch(i) replayed from CUDA graphs of
+    up to `batch` calls; returns (elapsed seconds, calls timed)."""
+    import torch
+    stream = torch.cuda.Stream()
+    for i in range(3):  # eager warm-up (per-kernel attributes, lazy module load)
+        with torch.cuda.stream(stream):
+            launch(i)
+    torch.cuda.synchronize()
+
+    def capture(n, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                launch(offset + i)
+        return g
+
+    b = min(batch, max(1, steps))
+    g_main = capture(b, 0)
+    tail = steps % b
+    g_tail = capture(tail, b) if tail else None
+    w_reps = max(1, (warmup + b - 1) // b)
+    for _ in range(w_reps):
+        g_main.replay()
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps // b):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / 1e3, steps
+
+
+def copies_for(nbytes: int, l2: int) -> int:
+    return max(1, -(-3 * l2 // max(1, nbytes)))
+
+
+# ---- our arm ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from mmvq_q2_gb300 import build as b
+    b.build()
+    import mmvq_q2_gb300 as q
+    L = q.lib()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    hbm, _, peak_src = peaks()
+
+    # headline workload
+    W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
+    x = synth.bf16_normal(0, "sweep.x1", (1, K_HEAD))
+    R = copies_for(W.nbytes, l2)
+    Wd0 = torch.from_numpy(W).cuda()
+    Ws = [Wd0] + [Wd0.clone() for _ in range(R - 1)]
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    yd = torch.empty((1, N_HEAD), dtype=torch.float32, device="cuda")
+    fn = L.q2k_gemv_bf16
+    wp = [ctypes.c_void_p(w.data_ptr()) for w in Ws]
+    xp, yp = ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(yd.data_ptr())
+
+    def launch(i):
+        st = fn(wp[i % R], N_HEAD, K_HEAD, xp, 1, K_HEAD, yp, N_HEAD,
+                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if st != 0:
+            raise RuntimeError(f"q2k_gemv_bf16 status {st}")
+
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    elapsed, n = graph_time(launch, args.steps, args.warmup)
+    ck = clocks.stop()
+    t_call = elapsed / n
+    tot_t, tot_bytes = aggregate(elapsed, float(n) * W_BYTES_HEAD)
+    value = tot_bytes / tot_t / 1e9
+    achieved = ALG_BYTES_HEAD / t_call / 1e9
+
+    # e2e through the C ABI with host buffers
+    Wh = torch.from_numpy(W).pin_memory()
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    yh = torch.empty((1, N_HEAD), dtype=torch.float32).pin_memory()
+    Wdev = torch.empty_like(Wd0)
+    xdev = torch.empty((1, K_HEAD), dtype=torch.int16, device="cuda")
+    e_steps = min(args.steps, 200)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(max(3, min(args.warmup, 10)) + e_steps):
+            if i == max(3, min(args.warmup, 10)):
+                torch.cuda.synchronize()
+                barrier()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+            Wdev.copy_(Wh, non_blocking=True)
+            xdev.copy_(xh, non_blocking=True)
+            st = fn(ctypes.c_void_p(Wdev.data_ptr()), N_HEAD, K_HEAD, ctypes.c_void_p(xdev.data_ptr()), 1, K_HEAD,
+                    yp, N_HEAD, ctypes.c_void_p(s.cuda_stream))
+            if st != 0:
+                raise RuntimeError(f"q2k_gemv_bf16 status {st}")
+            yh.copy_(yd, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    e_el, e_bytes = aggregate(e0.elapsed_time(e1) / 1e3, float(e_steps) * W_BYTES_HEAD)
+    e2e = {"value": e_bytes / e_el / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": int(W.nbytes + x.nbytes), "d2h_bytes_per_step": int(yh.numel() * 4),
+           "us_per_step": e_el / e_steps * 1e6}
+
+    # parity spot check of the timed output against the oracle (sampled rows)
+    import oracle
+    rows = np.arange(0, N_HEAD, 1021)
+    ref = oracle.matvec(np.ascontiguousarray(W[rows]), len(rows), K_HEAD,
+                        synth.bf16_bits_to_f32(x).astype(np.float64))
+    got = yd.cpu().numpy()[0, rows]
+    parity_err = float(np.max(np.abs(got - ref[0])) / np.linalg.norm(ref[0]))
+
+    line = None
+    if rank == 0:
+        cpu = cpu_baseline(W, x) if ws == 1 else None
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_call * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32 dot + f32 (Q2_K weights, bf16 activations)", "data": "synthetic",
+            "config": {"workload": "q2k_gemv_bf16 m=1 N=K=16384 (Q2_K weights, bf16 x, f32 y)",
+                       "weight_bytes": W_BYTES_HEAD, "l2": f"{R} rotating weight copies ({R * W.nbytes >> 20} MiB > 3x L2)",
+                       "graph_batch": 100, "parallelism": f"replicas x{ws}"},
+            "us_per_call": t_call * 1e6,
+            "tokens_per_s": 1.0 / t_call,
+            "frac_of_hbm_roofline_time": (ALG_BYTES_HEAD / (hbm * 1e9)) / t_call,
+            "clocks": ck,
+            "e2e": e2e,
+            "gpu_launches": n,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": committed_traffic(),
+                         "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                         "algorithmic_bytes_per_launch": ALG_BYTES_HEAD},
+            "parity_max_rel_err_sampled": parity_err,
+            "cpu_baseline": cpu,
+        }
+    if args.all:
+        sweep(q, L, l2, hbm, rank)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def cpu_baseline(W, x, budget_s: float = 20.0):
+    """The oracle (one thread) on a bounded sample of the headline workload:
+    rows of W until about budget_s seconds of CPU work."""
+    import oracle
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    rows = 64
+    t0 = time.perf_counter()
+    oracle.matvec(np.ascontiguousarray(W[:rows]), rows, K_HEAD, xf)
+    t_row = (time.perf_counter() - t0) / rows
+    n = int(min(N_HEAD, max(rows, budget_s / max(t_row, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.matvec(np.ascontiguousarray(W[:n]), n, K_HEAD, xf)
+    dt = time.perf_counter() - t0
+    return {"value": n * (K_HEAD // 256) * 84 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {N_HEAD} rows of the N=K=16384 m=1 workload ({dt:.1f} s)"}
+
+
+# ---- sweep over every configuration (--all) ------------------------------------------------
+
+def sweep(q, L, l2, hbm, rank):
+    import torch
+    out = []
+
+    def rec(name, t_call, nbytes, m, extra=None):
+        d = {"config": name, "us_per_call": t_call * 1e6, "bytes_per_call": int(nbytes),
+             "GBps": nbytes / t_call / 1e9, "frac_hbm": nbytes / t_call / 1e9 / hbm,
+             "tokens_per_s": m / t_call}
+        if extra:
+            d.update(extra)
+        out.append(d)
+        print(json.dumps(d), file=sys.stderr, flush=True)
+
+    cur = lambda: ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)  # noqa: E731
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    def check(st, name):
+        if st != 0:
+            raise RuntimeError(f"{name} status {st}")
+
+    # cfg0 and cfg4: Q2_K GEMV / MMVQ
+    shapes = [(512, 4096, (1,))] + [(n, n, (1, 2, 4, 8)) for n in (4096, 8192, 16384)]
+    for N, K, ms in shapes:
+        W = synth.q2k_matrix(0, f"sweep.W{N}x{K}", N, K)
+        R = copies_for(W.nbytes, l2)
+        W0 = torch.from_numpy(W).cuda()
+        Ws = [W0] + [W0.clone() for _ in range(R - 1)]
+        wp = [P(w) for w in Ws]
+        for m in ms:
+            x = synth.bf16_normal(0, f"sweep.x{m}.{K}", (m, K))
+            xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+            xq = q.q8_1_quantize_rows(xd)
+            y = torch.empty((m, N), dtype=torch.float32, device="cuda")
+            nb = W.nbytes
+            el, n = graph_time(lambda i: check(L.q2k_gemv_bf16(wp[i % R], N, K, P(xd), m, K, P(y), N, cur()), "gemv"),
+                               2000, 100)
+            rec(f"gemv_bf16 N={N} K={K} m={m}", el / n, nb + 2 * m * K + 4 * m * N, m)
+            el, n = graph_time(lambda i: check(L.q2k_mmvq_q8_1(wp[i % R], N, K, P(xq), m, P(y), N, cur()), "mmvq"),
+                               2000, 100)
+            rec(f"mmvq_q8_1 N={N} K={K} m={m}", el / n, nb + xq.numel() + 4 * m * N, m)
+        del Ws, W0
+        torch.cuda.empty_cache()
+
+    # cfg2: pair (q8_1 quantise + one launch for both)
+    K = 4096
+    Wa = synth.q2k_matrix(0, "cfg2.wq_a", 1024, K)
+    Wb = synth.q2k_matrix(0, "cfg2.wkv", 512, K)
+    R = copies_for(Wa.nbytes + Wb.nbytes, l2)
+    Was = [torch.from_numpy(Wa).cuda() for _ in range(R)]
+    Wbs = [torch.from_numpy(Wb).cuda() for _ in range(R)]
+    for m in (1, 4, 8):
+        x = synth.bf16_normal(0, f"cfg2.x{m}", (m, K))
+        xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        xq = torch.empty((m, q.q8_1_row_bytes(K)), dtype=torch.uint8, device="cuda")
+        ya = torch.empty((m, 1024), dtype=torch.float32, device="cuda")
+        yb = torch.empty((m, 512), dtype=torch.float32, device="cuda")
+
+        def pair(i):
+            check(L.q8_1_quantize_rows(P(xd), m, K, K, P(xq), cur()), "q8")
+            check(L.q2k_mmvq_pair(P(Was[i % R]), 1024, P(ya), P(Wbs[i % R]), 512, P(yb), K, P(xq), m, cur()), "pair")
+        el, n = graph_time(pair, 2000, 100)
+        rec(f"pair (q8_1 + wq_a/wkv) m={m}", el / n, Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
+    del Was, Wbs
+
+    # cfg3: routed experts for one token (256 experts resident, selection varies per call)
+    E_all, topk, dim, inter = 256, 8, 4096, 2048
+    mats = {}
+    for e in range(E_all):
+        for kind, shape in (("gate", (inter, dim)), ("up", (inter, dim)), ("down", (dim, inter))):
+            mats[(kind, e)] = torch.from_numpy(synth.q2k_matrix(0, f"cfg3.{kind}{e}", *shape)).cuda()
+    rng = np.random.default_rng(0)
+    tables = []
+    for _ in range(64):
+        sel = rng.choice(E_all, topk, replace=False)
+        tables.append(q.pointer_table([mats[("gate", int(e))] for e in sel] + [mats[("up", int(e))] for e in sel] +
+                                      [mats[("down", int(e))] for e in sel]))
+    x = synth.bf16_normal(0, "cfg3.x", (1, dim))
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    _, w = synth.expert_route(0, E_all, topk)
+    wd = torch.from_numpy(w).cuda()
+    yo = torch.empty(dim, dtype=torch.float32, device="cuda")
+    wsb = q.q2k_moe_m1_workspace_bytes(topk, dim, inter)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    el, n = graph_time(lambda i: check(L.q2k_moe_m1(P(tables[i % 64]), topk, dim, inter, P(xd), P(wd), P(yo), P(ws),
+                                                    wsb, cur()), "moe"), 1000, 50)
+    moe_bytes = 3 * topk * inter * (dim // 256) * 84
+    rec("moe_m1 (8 of 256 experts, gate/up -> SwiGLU -> down)", el / n, moe_bytes, 1, {"launches_per_call": 4})
+    del mats, tables
+    torch.cuda.empty_cache()
+
+    # cfg1: engram rows + GEMM m=16
+    n_table = 1 << 20
+    table = torch.from_numpy(synth.q2k_blocks(0, "cfg1.table", n_table)).cuda()
+    ids = torch.from_numpy(synth.row_ids(0, "cfg1.ids", 128, n_table)).cuda()
+    wkv = synth.bf16_normal(0, "cfg1.wkv", (20480, 2048), std=0.02)
+    R = copies_for(wkv.nbytes, l2)
+    wkvs = [torch.from_numpy(wkv.view(np.int16)).cuda() for _ in range(R)]
+    rows = torch.empty((128, 256), dtype=torch.int16, device="cuda")
+    yk = torch.empty((16, 20480), dtype=torch.float32, device="cuda")
+
+    def engram(i):
+        check(L.q2k_dequant_rows(P(table), n_table, 256, P(ids), 128, P(rows), None, cur()), "dequant")
+        check(L.dense_gemm_bf16(P(rows), 16, 2048, 2048, P(wkvs[i % R]), 20480, P(yk), 20480, cur()), "gemm")
+    el, n = graph_time(engram, 500, 20)
+    rec("engram rows(128) + dense_gemm m=16 [20480x2048]", el / n, wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 +
+        16 * 20480 * 4, 16)
+    del wkvs
+
+    # cfg4: dense GEMM m in {64, 256}
+    for Nn in (4096, 8192, 16384):
+        Wdn = synth.bf16_normal(0, f"sweep.dense.W{Nn}", (Nn, Nn), std=0.02)
+        R = copies_for(Wdn.nbytes, l2)
+        Wds = [torch.from_numpy(Wdn.view(np.int16)).cuda() for _ in range(R)]
+        for m in (64, 256):
+            xx = torch.from_numpy(synth.bf16_normal(0, f"sweep.dense.x{m}.{Nn}", (m, Nn)).view(np.int16)).cuda()
+            yy = torch.empty((m, Nn), dtype=torch.float32, device="cuda")
+            el, n = graph_time(lambda i: check(L.dense_gemm_bf16(P(xx), m, Nn, Nn, P(Wds[i % R]), Nn, P(yy), Nn, cur()),
+                                               "gemm"), 200, 10)
+            flops = 2.0 * m * Nn * Nn
+            rec(f"dense_gemm_bf16 m={m} N=K={Nn}", el / n, Wdn.nbytes + 2 * m * Nn + 4 * m * Nn, m,
+                {"TFLOPs": flops / (el / n) / 1e12})
+        del Wds
+        torch.cuda.empty_cache()
+
+    if rank == 0 and os.path.isdir(os.path.join(ROOT, "gpurun_out")):
+        with open(os.path.join(ROOT, "gpurun_out", "bench_all.jsonl"), "w") as f:
+            for d in out:
+                f.write(json.dumps(d) + "\n")
+
+
+# ---- reference arm: the CPU oracle -------------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
+    x = synth.bf16_normal(0, "sweep.x1", (1, K_HEAD))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.matvec(np.ascontiguousarray(W[:16]), 16, K_HEAD, xf)
+    t_row = (time.perf_counter() - t0) / 16
+    budget = 150.0  # seconds for warm-up + timed steps together
+    rows = int(max(1, min(N_HEAD, budget / max(1, args.steps + args.warmup) / max(t_row, 1e-9))))
+    sample = np.ascontiguousarray(W[:rows])
+    for _ in range(args.warmup):
+        oracle.matvec(sample, rows, K_HEAD, xf)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matvec(sample, rows, K_HEAD, xf)
+    dt = time.perf_counter() - t0
+    value = args.steps * rows * (K_HEAD // 256) * 84 / dt / 1e9
+    desc = f"{rows} of {N_HEAD} rows of the N=K=16384 m=1 workload per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "q2k_gemv_bf16 m=1 N=K=16384 (Q2_K weights, bf16 x) - CPU oracle sample",
+                   "parallelism": "single host thread"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--all", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * q2k.h -- C ABI of the Q2_K decode-projection library (libq2k.so).
+ *
+ * Decode-time projections read straight off GGUF Q2_K weight blocks, for
+ * m <= 8 tokens, with bf16 or q8_1 activations, on one NVIDIA GB300
+ * (sm_103a).  Sources are the metrale docs pages (engram_v41.rs,
+ * engram_v41/apply.rs, attn_v41/decode.rs, moe_v41/init.rs); each entry
+ * point cites the item it follows.
+ *
+ * Conventions (engram_v41/apply.rs `apply` and attn_v41/decode.rs
+ * `q_kv_projections`: raw device pointers, integer shapes, a stream; every
+ * check before any launch):
+ *  - Every pointer argument is a DEVICE pointer unless its comment says
+ *    otherwise.  The caller owns every buffer; the library never allocates,
+ *    frees or synchronises, and keeps no state besides per-device launch
+ *    tuning read from the device once.  All work is enqueued on `stream`
+ *    (NULL = the legacy default stream); calls return before it runs.
+ *  - Arguments are validated before anything is enqueued.  A non-zero
+ *    status means nothing was launched (Q2K_ERR_CUDA: a launch was refused
+ *    by the runtime; its error is reported by q2k_last_cuda_error()).
+ *  - Weights: row-major [N, K] as GGUF ships them, K/256 super-blocks per
+ *    row (engram_v41.rs, `wkv_q2k`: `[out, in / 256]` blocks).  y = x W^T.
+ *  - Activations: bf16 (raw uint16 bit patterns) or q8_1 rows.
+ *  - Outputs: fp32 unless stated.
+ *
+ * Q2_K super-block, 84 bytes, 256 weights (engram_v41.rs,
+ * `ENGRAM_ROW_BYTES`), read as the GGUF Q2_K layout:
+ *     bytes  0..15  scales[16]: sub-block j = p/16; low nibble = scale,
+ *                   high nibble = min
+ *     bytes 16..79  qs[64]: weight p's 2-bit code q_p is bits
+ *                   2*((p%128)/32)..+1 of qs[32*(p/128) + p%32]
+ *     bytes 80..81  d    (fp16, little endian)
+ *     bytes 82..83  dmin (fp16, little endian)
+ *     w_p = d * (scales[j] & 15) * q_p - dmin * (scales[j] >> 4)
+ *
+ * q8_1 block, 36 bytes, 32 values (the library's own layout; attn_v41 and
+ * moe_v41 name the format only):
+ *     bytes 0..1 d (fp16), bytes 2..3 s (fp16), bytes 4..35 q[32] (int8)
+ *     d32 = amax/127 (fp32 divide), q = round_half_away(x/d32),
+ *     d = fp16(d32), s = fp16(f32(d) * sum(q)).  Rows are K/32 blocks,
+ *     contiguous, rows back to back.
+ *
+ * Alignment: weights and q8_1 rows must be 4-byte aligned, bf16 arrays
+ * 2-byte aligned, fp32 arrays 4-byte aligned (Q2K_ERR_MISALIGNED).
+ * Weight rows that start on 16-byte boundaries (K % 1024 == 0 and a 16-byte
+ * aligned base) are streamed with bulk asynchronous copies; other rows take
+ * a slower copy path with identical results.
+ */
+#ifndef Q2K_H
+#define Q2K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* q2k_stream_t;
+
+enum q2k_status {
+    Q2K_OK = 0,
+    Q2K_ERR_NULL_ARG = 1,    /* a required pointer is NULL */
+    Q2K_ERR_BAD_SHAPE = 2,   /* K % 256 != 0, m outside 1..8, N <= 0, ... */
+    Q2K_ERR_MISALIGNED = 3,  /* a pointer below its required alignment */
+    Q2K_ERR_CUDA = 4,        /* the CUDA runtime refused a query or launch */
+    Q2K_ERR_UNSUPPORTED = 5, /* current device is not compute capability 10.3 */
+    Q2K_ERR_WORKSPACE = 6    /* workspace NULL or smaller than required */
+};
+
+/* Bytes of one Q2_K row of K weights: K/256*84, or 0 when K % 256 != 0. */
+size_t q2k_row_bytes(int64_t K);
+
+/* Bytes of one q8_1 row of K values: K/32*36, or 0 when K % 32 != 0
+ * (moe_v41/init.rs, `kquant_q8_1_rows_bytes`). */
+size_t q8_1_row_bytes(int64_t K);
+
+/* Gather + dequantise Q2_K rows to bf16 (engram_v41.rs, `rows_from_q2k`
+ * and `dequant_q2_k_to_bf16`; the gather of rows by id is done on the
+ * device instead of on the host).
+ *   table         Q2_K rows, [n_table_rows, K/256] blocks
+ *   ids           int32 [n_rows] row ids into table, or NULL for rows
+ *                 0..n_rows-1 (then n_rows <= n_table_rows)
+ *   out_bf16      [n_rows, K] bf16, row r = decode(table[ids[r]]), each
+ *                 weight computed in fp32 and rounded once to bf16 (RN)
+ *   err_flag      int32, nullable: set to 1 when an id is outside
+ *                 [0, n_table_rows); that row is written as zeros
+ * Engram rows are K = 256 (one block per row) in [token][col] order. */
+int q2k_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids,
+                     int64_t n_rows, uint16_t* out_bf16, int32_t* err_flag, q2k_stream_t stream);
+
+/* Quantise bf16 rows to q8_1 (attn_v41/decode.rs, `kquant_q8_1_rows`;
+ * moe_v41/init.rs, `kquant_q8_1_rows_bf16`).
+ *   x_bf16   [m, K] with row stride ldx elements (ldx >= K); K % 32 == 0
+ *   out_q8_1 m * q8_1_row_bytes(K) bytes
+ * q and d are bit-exact to the encoding in this header's preamble. */
+int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx, void* out_q8_1,
+                       q2k_stream_t stream);
+
+/* Q2_K GEMV with bf16 activations, m = 1..8 tokens (engram_v41/apply.rs,
+ * the single-token `engram_v41_wkv_q2k_gemv` off `wkv_q2k`).
+ *   W  Q2_K [N, K];  x  bf16 [m, K], row stride ldx;  y  fp32 [m, N], row
+ *   stride ldy.  y[t, n] = sum_k w[n, k] x[t, k], fp32 accumulation.
+ * The activations enter the integer dot products as 16-bit fixed point
+ * with one power-of-two exponent per 16 values (exact unless a group spans
+ * more than 2^7 in magnitude; then the smallest lose bits below 2^-15 of
+ * the group maximum); groups below 2^-100 in magnitude count as zero. */
+int q2k_gemv_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx,
+                  float* y, int64_t ldy, q2k_stream_t stream);
+
+/* Q2_K x q8_1 MMVQ, m = 1..8 (moe_v41/init.rs, `kquant_mmvq_q2_k_w`).
+ *   W Q2_K [N, K];  xq  m q8_1 rows of K values;  y fp32 [m, N], stride ldy.
+ * Per sub-block: d*sc*d8*sum(q*q8) - dmin*m*d8*sum(q8), in fp32. */
+int q2k_mmvq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y,
+                  int64_t ldy, q2k_stream_t stream);
+
+/* Two Q2_K matrices over one q8_1 input in a single launch (attn_v41/
+ * decode.rs, `kquant_mmvq_pair_w`: `wq_a` -> `qr_raw`, `wkv` -> `kv_raw`).
+ *   Wa [Na, K] -> ya fp32 [m, Na];  Wb [Nb, K] -> yb fp32 [m, Nb]
+ * Each output equals q2k_mmvq_q8_1 of its matrix bit for bit. */
+int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb,
+                  int64_t K, const void* xq, int64_t m, q2k_stream_t stream);
+
+/* Batched single-token MMVQ over n_mat Q2_K matrices of one shape, with an
+ * optional fused route-weighted sum (moe_v41/init.rs,
+ * `kquant_mmvq_q2_k_experts_w8`, `moe_v41_accumulate`).
+ *   W_table      device array of n_mat device pointers, each Q2_K [N, K]
+ *   xq           q8_1 input: one row shared by every matrix
+ *                (x_per_matrix == 0) or row e for matrix e (x_per_matrix
+ *                == 1, rows back to back)
+ *   y            fp32 [n_mat, N], nullable when y_sum is given; row e
+ *                equals q2k_mmvq_q8_1(W_table[e], xq row) bit for bit
+ *   route_w      fp32 [n_mat], required with y_sum
+ *   y_sum        fp32 [N], nullable: y_sum[n] = sum_e route_w[e]*y[e,n],
+ *                added in e order (deterministic)
+ * Gate and up run as one batch of 2*topk matrices; down as topk matrices
+ * with x_per_matrix = 1 (moe_v41/init.rs, the `gate_out` comment). */
+int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K,
+                     const void* xq, int x_per_matrix, float* y, const float* route_w,
+                     float* y_sum, q2k_stream_t stream);
+
+/* SwiGLU fused with q8_1 requantisation (moe_v41/init.rs,
+ * `kquant_swiglu_q8_1_rows_bf16`).
+ *   gate_up  fp32 [2E, N]: gate rows 0..E-1, up rows E..2E-1 (the layout
+ *            q2k_mmvq_experts writes for a 2E gate+up batch)
+ *   h_q8     E q8_1 rows of N values;  h_bf16 [E, N] bf16, nullable
+ * g and u are first rounded to bf16 (the page's expert buffers are bf16),
+ * h = silu(g)*u in fp32 (silu(z) = z/(1+e^-z), expf) rounded to bf16, then
+ * q8_1-encoded.  N % 32 == 0. */
+int swiglu_q8_1_rows(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16,
+                     q2k_stream_t stream);
+
+/* Workspace bytes q2k_moe_m1 needs for E experts (256-byte aligned parts). */
+size_t q2k_moe_m1_workspace_bytes(int64_t E, int64_t dim, int64_t inter);
+
+/* The routed-expert step for one token as one call (moe_v41/init.rs): q8_1
+ * of x, the 2E gate+up batch, SwiGLU + q8_1 of h, the E down batch with
+ * the route-weighted sum.  Four launches on `stream`.
+ *   ptrs      device array of 3E device pointers: gate_0..gate_{E-1}
+ *             ([inter, dim] each), up_0..up_{E-1} ([inter, dim]),
+ *             down_0..down_{E-1} ([dim, inter]) (moe_v41/init.rs, `ptrs_dev`)
+ *   x_bf16    [dim];  route_w fp32 [E];  y fp32 [dim]
+ *   workspace at least q2k_moe_m1_workspace_bytes(E, dim, inter) bytes,
+ *             256-byte aligned; its contents on return are the q8_1 x, the
+ *             fp32 gate/up outputs and the q8_1 h, in that order. */
+int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
+               const uint16_t* x_bf16, const float* route_w, float* y, void* workspace,
+               size_t workspace_bytes, q2k_stream_t stream);
+
+/* Dense bf16 GEMM on the tensor cores, any m >= 1 (engram_v41/apply.rs,
+ * `ops::dense_gemm` for several tokens; moe_v41/init.rs `dense_gemm_bf16`).
+ *   x bf16 [m, K], row stride ldx;  W bf16 [N, K] row-major;
+ *   y fp32 [m, N], row stride ldy.  K % 8 == 0; x, W 16-byte aligned and
+ *   ldx % 8 == 0.  fp32 accumulation.  When the library splits K across
+ *   thread blocks (small N), partial sums are added with fp32 atomics, so
+ *   the last bits may differ between runs. */
+int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
+                    int64_t N, float* y, int64_t ldy, q2k_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* q2k_status_string(int status);
+
+/* The last CUDA runtime error code a call returned as Q2K_ERR_CUDA in
+ * this thread (0 if none). */
+int q2k_last_cuda_error(void);
+
+/* Diagnostics, synchronous (not for use inside stream capture): reads the
+ * device's library error word into *host_out (0 = none; bit 0 = a bounded
+ * wait in a kernel gave up and that kernel returned early, outputs
+ * incomplete) and clears it when clear != 0. */
+int q2k_device_error(int32_t* host_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q2K_H */

@@ -1,0 +1,376 @@
+// C ABI entry points (include/q2k.h): argument validation before any CUDA
+// call, then dispatch to the kernel translation units.  Validation mirrors
+// the pages' `ensure!` checks that run before any launch
+// (engram_v41/apply.rs `apply`, engram_v41.rs `rows_from_q2k`,
+// moe_v41/init.rs `MoeV41::new`).
+#include "../../include/q2k.h"
+#include "q2k_common.cuh"
+#include "q2k_internal.h"
+
+#include <mutex>
+
+namespace q2k {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+std::mutex g_info_mu;
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    return Q2K_ERR_CUDA;
+}
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(g_info_mu);
+        if (g_info_ok[dev]) {
+            *out = g_info[dev];
+            return cudaSuccess;
+        }
+    }
+    DeviceInfo d{};
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_info_mu);
+    g_info[dev] = d;
+    g_info_ok[dev] = true;
+    *out = d;
+    return cudaSuccess;
+}
+
+}  // namespace q2k
+
+using namespace q2k;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Device check: compute capability 10.3 (the library carries sm_103a code only).
+int check_device()
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    if (di.cc_major != 10 || di.cc_minor != 3)
+        return Q2K_ERR_UNSUPPORTED;
+    return Q2K_OK;
+}
+
+int finish(cudaError_t e) { return e == cudaSuccess ? Q2K_OK : fail_cuda(e); }
+
+// Largest K the library accepts (weights rows up to 1 MiB of blocks).
+constexpr int64_t kMaxK = 1 << 20;
+
+}  // namespace
+
+extern "C" {
+
+size_t q2k_row_bytes(int64_t K)
+{
+    if (K <= 0 || K % kBlockWeights)
+        return 0;
+    return (size_t)(K / kBlockWeights) * kBlockBytes;
+}
+
+size_t q8_1_row_bytes(int64_t K)
+{
+    if (K <= 0 || K % kQ8Values)
+        return 0;
+    return (size_t)(K / kQ8Values) * kQ8Bytes;
+}
+
+const char* q2k_status_string(int status)
+{
+    switch (status) {
+    case Q2K_OK: return "ok";
+    case Q2K_ERR_NULL_ARG: return "null argument";
+    case Q2K_ERR_BAD_SHAPE: return "bad shape";
+    case Q2K_ERR_MISALIGNED: return "misaligned pointer";
+    case Q2K_ERR_CUDA: return "cuda runtime error";
+    case Q2K_ERR_UNSUPPORTED: return "unsupported device (needs compute capability 10.3)";
+    case Q2K_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int q2k_last_cuda_error(void) { return t_last_cuda_error; }
+
+int q2k_device_error(int32_t* host_out, int clear)
+{
+    if (!host_out)
+        return Q2K_ERR_NULL_ARG;
+    int32_t a = 0, b = 0;
+    cudaError_t e = mv_error_word(&a, clear != 0);
+    if (e == cudaSuccess)
+        e = gemm_error_word(&b, clear != 0);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    *host_out = a | b;
+    return Q2K_OK;
+}
+
+int q2k_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids, int64_t n_rows,
+                     uint16_t* out_bf16, int32_t* err_flag, q2k_stream_t stream)
+{
+    if (!table || !out_bf16)
+        return Q2K_ERR_NULL_ARG;
+    if (K <= 0 || K % kBlockWeights || K > kMaxK || n_rows < 0 || n_table_rows <= 0)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!ids && n_rows > n_table_rows)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(table, 4) || !aligned(out_bf16, 2) || (ids && !aligned(ids, 4)) || (err_flag && !aligned(err_flag, 4)))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (n_rows == 0)
+        return Q2K_OK;
+    return finish(launch_dequant_rows(table, n_table_rows, K, ids, n_rows, out_bf16, err_flag,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx, void* out_q8_1,
+                       q2k_stream_t stream)
+{
+    if (!x_bf16 || !out_q8_1)
+        return Q2K_ERR_NULL_ARG;
+    if (m < 0 || K <= 0 || K % kQ8Values || ldx < K || K > kMaxK)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(x_bf16, 2) || !aligned(out_q8_1, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (m == 0)
+        return Q2K_OK;
+    return finish(launch_q8_1_quantize(x_bf16, m, K, ldx, out_q8_1, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q2k_gemv_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx, float* y,
+                  int64_t ldy, q2k_stream_t stream)
+{
+    if (!W || !x || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (N <= 0 || K <= 0 || K % kBlockWeights || K > kMaxK || m < 1 || m > 8 || ldx < K || ldy < N)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W, 4) || !aligned(x, 2) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    MvProblem p{};
+    p.act = ACT_BF16;
+    p.m = (int)m;
+    p.K = K;
+    p.n_seg = 1;
+    p.W[0] = W;
+    p.N[0] = N;
+    p.y[0] = y;
+    p.ldy[0] = ldy;
+    p.x = x;
+    p.x_tok_stride = ldx * 2;
+    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q2k_mmvq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y, int64_t ldy,
+                  q2k_stream_t stream)
+{
+    if (!W || !xq || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (N <= 0 || K <= 0 || K % kBlockWeights || K > kMaxK || m < 1 || m > 8 || ldy < N)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W, 4) || !aligned(xq, 4) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = (int)m;
+    p.K = K;
+    p.n_seg = 1;
+    p.W[0] = W;
+    p.N[0] = N;
+    p.y[0] = y;
+    p.ldy[0] = ldy;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb, int64_t K,
+                  const void* xq, int64_t m, q2k_stream_t stream)
+{
+    if (!Wa || !Wb || !ya || !yb || !xq)
+        return Q2K_ERR_NULL_ARG;
+    if (Na <= 0 || Nb <= 0 || K <= 0 || K % kBlockWeights || K > kMaxK || m < 1 || m > 8)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(Wa, 4) || !aligned(Wb, 4) || !aligned(ya, 4) || !aligned(yb, 4) || !aligned(xq, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = (int)m;
+    p.K = K;
+    p.n_seg = 2;
+    p.W[0] = Wa;
+    p.W[1] = Wb;
+    p.N[0] = Na;
+    p.N[1] = Nb;
+    p.y[0] = ya;
+    p.y[1] = yb;
+    p.ldy[0] = Na;
+    p.ldy[1] = Nb;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K, const void* xq,
+                     int x_per_matrix, float* y, const float* route_w, float* y_sum, q2k_stream_t stream)
+{
+    if (!W_table || !xq || (!y && !y_sum) || (y_sum && !route_w))
+        return Q2K_ERR_NULL_ARG;
+    if (n_mat <= 0 || n_mat > 4096 || N <= 0 || K <= 0 || K % kBlockWeights || K > kMaxK ||
+        (x_per_matrix != 0 && x_per_matrix != 1))
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W_table, 8) || !aligned(xq, 4) || (y && !aligned(y, 4)) || (route_w && !aligned(route_w, 4)) ||
+        (y_sum && !aligned(y_sum, 4)))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = 1;
+    p.K = K;
+    p.n_seg = (int)n_mat;
+    p.W_table = W_table;
+    p.N[0] = N;
+    p.y_exp = y;
+    p.route_w = route_w;
+    p.y_sum = y_sum;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    p.x_seg_stride = x_per_matrix ? (int64_t)q8_1_row_bytes(K) : 0;
+    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int swiglu_q8_1_rows(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16, q2k_stream_t stream)
+{
+    if (!gate_up || !h_q8)
+        return Q2K_ERR_NULL_ARG;
+    if (E <= 0 || N <= 0 || N % kQ8Values || N > kMaxK)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(gate_up, 4) || !aligned(h_q8, 4) || (h_bf16 && !aligned(h_bf16, 2)))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    return finish(launch_swiglu_q8_1(gate_up, E, N, h_q8, h_bf16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t q2k_moe_m1_workspace_bytes(int64_t E, int64_t dim, int64_t inter)
+{
+    if (E <= 0 || dim <= 0 || inter <= 0 || dim % kBlockWeights || inter % kBlockWeights)
+        return 0;
+    return round256(q8_1_row_bytes(dim)) + round256((size_t)2 * E * inter * sizeof(float)) +
+           round256((size_t)E * q8_1_row_bytes(inter));
+}
+
+int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, const uint16_t* x_bf16,
+               const float* route_w, float* y, void* workspace, size_t workspace_bytes, q2k_stream_t stream)
+{
+    if (!ptrs || !x_bf16 || !route_w || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (E <= 0 || E > 1024 || dim <= 0 || inter <= 0 || dim % kBlockWeights || inter % kBlockWeights ||
+        dim > kMaxK || inter > kMaxK)
+        return Q2K_ERR_BAD_SHAPE;
+    const size_t need = q2k_moe_m1_workspace_bytes(E, dim, inter);
+    if (!workspace || workspace_bytes < need)
+        return Q2K_ERR_WORKSPACE;
+    if (!aligned(ptrs, 8) || !aligned(x_bf16, 2) || !aligned(route_w, 4) || !aligned(y, 4) || !aligned(workspace, 256))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* xq = ws;
+    float* gate_up = reinterpret_cast<float*>(ws + round256(q8_1_row_bytes(dim)));
+    void* h_q8 = ws + round256(q8_1_row_bytes(dim)) + round256((size_t)2 * E * inter * sizeof(float));
+    cudaError_t e = launch_q8_1_quantize(x_bf16, 1, dim, dim, xq, s);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = 1;
+    p.K = dim;
+    p.n_seg = (int)(2 * E);
+    p.W_table = ptrs;
+    p.N[0] = inter;
+    p.y_exp = gate_up;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(dim);
+    p.x_seg_stride = 0;
+    if ((e = launch_mv(p, s)) != cudaSuccess)
+        return fail_cuda(e);
+    if ((e = launch_swiglu_q8_1(gate_up, E, inter, h_q8, nullptr, s)) != cudaSuccess)
+        return fail_cuda(e);
+    MvProblem d{};
+    d.act = ACT_Q8;
+    d.m = 1;
+    d.K = inter;
+    d.n_seg = (int)E;
+    d.W_table = ptrs + 2 * E;
+    d.N[0] = dim;
+    d.y_exp = nullptr;
+    d.route_w = route_w;
+    d.y_sum = y;
+    d.x = h_q8;
+    d.x_tok_stride = (int64_t)q8_1_row_bytes(inter);
+    d.x_seg_stride = (int64_t)q8_1_row_bytes(inter);
+    return finish(launch_mv(d, s));
+}
+
+int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W, int64_t N, float* y,
+                    int64_t ldy, q2k_stream_t stream)
+{
+    if (!x || !W || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (m < 1 || K <= 0 || K % 8 || N <= 0 || ldx < K || ldx % 8 || ldy < N || K > (1 << 30) / 2 ||
+        N > (1 << 30) || m > (1 << 24))
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    return finish(launch_dense_gemm(x, m, K, ldx, W, N, y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

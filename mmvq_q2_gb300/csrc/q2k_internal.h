@@ -1,0 +1,57 @@
+// Host-side interface between the C-ABI layer (q2k_api.cu) and the kernel
+// translation units.  Shapes arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q2k {
+
+enum Act : int { ACT_BF16 = 0, ACT_Q8 = 1 };
+
+// Per-device facts read once (multiprocessor count, shared memory limit).
+struct DeviceInfo {
+    int sm_count;
+    int smem_optin;  // max dynamic shared memory per block (bytes)
+    int cc_major, cc_minor;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+// One GEMV/MMVQ problem.  Segments are weight matrices sharing K.
+//  - explicit segments (n_seg 1 or 2): W[e], N[e], y[e] + t*ldy[e]
+//  - table segments (W_table != null, experts): n_seg matrices of N[0] rows,
+//    y_exp [n_seg, N], optional route-weighted y_sum [N]; m == 1.
+struct MvProblem {
+    int act;  // Act
+    int m;
+    int64_t K;
+    int n_seg;
+    const void* const* W_table;
+    const void* W[2];
+    int64_t N[2];
+    float* y[2];
+    int64_t ldy[2];
+    float* y_exp;
+    const float* route_w;
+    float* y_sum;
+    const void* x;           // bf16 elements or q8_1 bytes
+    int64_t x_tok_stride;    // bytes between tokens
+    int64_t x_seg_stride;    // bytes between segments' inputs (0 = shared)
+};
+
+cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
+
+cudaError_t launch_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids,
+                                int64_t n_rows, uint16_t* out, int32_t* err_flag, cudaStream_t s);
+cudaError_t launch_q8_1_quantize(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, void* out,
+                                 cudaStream_t s);
+cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16,
+                               cudaStream_t s);
+cudaError_t launch_dense_gemm(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
+                              int64_t N, float* y, int64_t ldy, cudaStream_t s);
+
+// Read (and optionally clear) this translation unit's device error word.
+cudaError_t mv_error_word(int32_t* out, bool clear);
+cudaError_t gemm_error_word(int32_t* out, bool clear);
+
+}  // namespace q2k

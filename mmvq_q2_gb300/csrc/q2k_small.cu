@@ -1,0 +1,213 @@
+// Small memory-bound kernels around the projections:
+//  - gather + dequantise Q2_K rows to bf16 (engram_v41.rs, `rows_from_q2k`,
+//    `dequant_q2_k_to_bf16`), with the row gather moved onto the device;
+//  - bf16 -> q8_1 rows (attn_v41/decode.rs, `kquant_q8_1_rows`);
+//  - SwiGLU fused with q8_1 requantisation (moe_v41/init.rs,
+//    `kquant_swiglu_q8_1_rows_bf16`).
+#include "q2k_common.cuh"
+#include "q2k_internal.h"
+
+#include <algorithm>
+
+namespace q2k {
+
+// ---- dequant ----------------------------------------------------------------
+// One thread per 8 consecutive weights p = 8l..8l+7 of a block (l = 0..31):
+// they share half n = l/16, pair j = (l%16)/4, sub-block l/2, and take qs
+// bytes 32n + 8(l%4) .. +7 at bit shift 2j.
+template <bool VEC16>
+__global__ void __launch_bounds__(256) q2k_dequant_kernel(const uint8_t* __restrict__ table, int64_t n_table_rows,
+                                                          int nb, const int32_t* __restrict__ ids, int64_t n_rows,
+                                                          uint16_t* __restrict__ out, int32_t* err_flag)
+{
+    const int64_t total = n_rows * nb * 32;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+        const int l = (int)(u & 31);
+        const int64_t bi = u >> 5;
+        const int64_t r = bi / nb;
+        const int b = (int)(bi - r * nb);
+        const int64_t src = ids ? (int64_t)ids[r] : r;
+        uint16_t* o = out + (r * nb + b) * kBlockWeights + 8 * l;
+        uint32_t packed[4];
+        if (src < 0 || src >= n_table_rows) {
+            packed[0] = packed[1] = packed[2] = packed[3] = 0u;
+            if (err_flag && l == 0)
+                atomicExch(err_flag, 1);
+        } else {
+            const uint8_t* blk = table + (src * nb + b) * kBlockBytes;
+            const int n = l >> 4, j = (l & 15) >> 2, sb = l >> 1;
+            const uint32_t dm = ldg32_nc(blk + 80);
+            const uint32_t scw = ldg32_nc(blk + (sb & ~3));
+            const uint32_t scb = (scw >> (8 * (sb & 3))) & 0xFFu;
+            const float dl = half_lo_f(dm) * (float)(scb & 15u);  // exact
+            const float ml = half_hi_f(dm) * (float)(scb >> 4);   // exact
+            const uint8_t* qp = blk + 16 + 32 * n + 8 * (l & 3);
+            const uint32_t q0 = ldg32_nc(qp), q1 = ldg32_nc(qp + 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = i < 2 ? q0 : q1;
+                const int bA = (2 * i) & 3, bB = (2 * i + 1) & 3;
+                const float qa = (float)((w >> (8 * bA + 2 * j)) & 3u);
+                const float qb = (float)((w >> (8 * bB + 2 * j)) & 3u);
+                // one rounding to fp32 (dl*q is exact), then one to bf16
+                const __nv_bfloat16 ha = __float2bfloat16_rn(fmaf(dl, qa, -ml));
+                const __nv_bfloat16 hb = __float2bfloat16_rn(fmaf(dl, qb, -ml));
+                packed[i] = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+            }
+        }
+        if constexpr (VEC16) {
+            *reinterpret_cast<uint4*>(o) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o[2 * i] = (uint16_t)(packed[i] & 0xFFFFu);
+                o[2 * i + 1] = (uint16_t)(packed[i] >> 16);
+            }
+        }
+    }
+}
+
+cudaError_t launch_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids,
+                                int64_t n_rows, uint16_t* out, int32_t* err_flag, cudaStream_t s)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    const int nb = (int)(K / kBlockWeights);
+    const int64_t threads = n_rows * nb * 32;
+    const int64_t grid = std::min<int64_t>((threads + 255) / 256, (int64_t)di.sm_count * 8);
+    const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    if (vec)
+        q2k_dequant_kernel<true><<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t*>(table), n_table_rows, nb,
+                                                            ids, n_rows, out, err_flag);
+    else
+        q2k_dequant_kernel<false><<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t*>(table), n_table_rows, nb,
+                                                             ids, n_rows, out, err_flag);
+    return cudaGetLastError();
+}
+
+// ---- q8_1 ---------------------------------------------------------------------
+// Eight lanes per 32-value block, four values per lane.  amax, d32 = amax/127
+// and q = round(x/d32) use IEEE fp32 division (explicit __fdiv_rn) and
+// round-half-away-from-zero, so q and d are bit-exact to the encoding.
+// Every lane of the warp calls this (dead lanes with live == false and
+// zeros) so that the shuffles stay converged; only live lanes store.
+__device__ __forceinline__ void q8_1_encode_group(const float (&v)[4], uint8_t* blk, int lane8, bool live)
+{
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d32 = __fdiv_rn(amax, 127.0f);
+    int q[4];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[i] = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v[i], d32));
+        sum += q[i];
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const __half dh = __float2half_rn(d32);
+    const __half sh = __float2half_rn(__fmul_rn(__half2float(dh), (float)sum));
+    const uint32_t qw = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
+                        ((uint32_t)(q[3] & 0xFF) << 24);
+    if (!live)
+        return;
+    *reinterpret_cast<uint32_t*>(blk + 4 + 4 * lane8) = qw;
+    if (lane8 == 0)
+        *reinterpret_cast<uint32_t*>(blk) =
+            (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(sh) << 16);
+}
+
+__global__ void __launch_bounds__(256) q8_1_quantize_kernel(const uint16_t* __restrict__ x, int64_t m, int nblk,
+                                                            int64_t ldx, uint8_t* __restrict__ out)
+{
+    const int64_t total = m * nblk * 8;  // lanes
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // every lane of a warp must reach the shuffles: iterate a warp-uniform count
+    const int64_t base0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+    for (int64_t wbase = base0; wbase < total; wbase += stride) {
+        const int64_t u = wbase + (threadIdx.x & 31);
+        const bool live = u < total;
+        const int64_t uu = live ? u : wbase;
+        const int lane8 = (int)(uu & 7);
+        const int64_t bi = uu >> 3;
+        const int64_t t = bi / nblk;
+        const int b = (int)(bi - t * nblk);
+        const uint16_t* xp = x + t * ldx + (int64_t)b * kQ8Values + 4 * lane8;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = live ? bf16_bits_f(xp[i]) : 0.f;
+        q8_1_encode_group(v, out + (t * nblk + b) * kQ8Bytes, lane8, live);
+    }
+}
+
+cudaError_t launch_q8_1_quantize(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, void* out, cudaStream_t s)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    const int nblk = (int)(K / kQ8Values);
+    const int64_t lanes = m * nblk * 8;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((lanes + 255) / 256, (int64_t)di.sm_count * 8));
+    q8_1_quantize_kernel<<<(int)grid, 256, 0, s>>>(x, m, nblk, ldx, static_cast<uint8_t*>(out));
+    return cudaGetLastError();
+}
+
+// ---- SwiGLU + q8_1 --------------------------------------------------------------
+__global__ void __launch_bounds__(256) swiglu_q8_1_kernel(const float* __restrict__ gate_up, int64_t E, int64_t N,
+                                                          uint8_t* __restrict__ h_q8, uint16_t* __restrict__ h_bf16)
+{
+    const int nblk = (int)(N / kQ8Values);
+    const int64_t total = E * nblk * 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t base0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+    for (int64_t wbase = base0; wbase < total; wbase += stride) {
+        const int64_t u = wbase + (threadIdx.x & 31);
+        const bool live = u < total;
+        const int64_t uu = live ? u : wbase;
+        const int lane8 = (int)(uu & 7);
+        const int64_t bi = uu >> 3;
+        const int64_t e = bi / nblk;
+        const int b = (int)(bi - e * nblk);
+        const int64_t k0 = (int64_t)b * kQ8Values + 4 * lane8;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float hv = 0.f;
+            if (live) {
+                // g, u rounded to bf16 first (bf16 expert buffers), then
+                // h = silu(g) * u in fp32, rounded to bf16.
+                const float g = __bfloat162float(__float2bfloat16_rn(gate_up[e * N + k0 + i]));
+                const float uv = __bfloat162float(__float2bfloat16_rn(gate_up[(E + e) * N + k0 + i]));
+                const float silu = __fdiv_rn(g, 1.0f + expf(-g));
+                const __nv_bfloat16 hb = __float2bfloat16_rn(__fmul_rn(silu, uv));
+                hv = __bfloat162float(hb);
+                if (h_bf16)
+                    h_bf16[e * N + k0 + i] = __bfloat16_as_ushort(hb);
+            }
+            v[i] = hv;
+        }
+        q8_1_encode_group(v, h_q8 + (e * nblk + b) * kQ8Bytes, lane8, live);
+    }
+}
+
+cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16,
+                               cudaStream_t s)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t lanes = E * (N / kQ8Values) * 8;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((lanes + 255) / 256, (int64_t)di.sm_count * 8));
+    swiglu_q8_1_kernel<<<(int)grid, 256, 0, s>>>(gate_up, E, N, static_cast<uint8_t*>(h_q8), h_bf16);
+    return cudaGetLastError();
+}
+
+}  // namespace q2k

@@ -39,8 +39,9 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
     Only used to build inputs; NaN never occurs in the drawn data."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = a.view(np.uint32)
+    # finite values stay below 0xFF800000, so the 32-bit sum cannot wrap
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return u.astype(np.uint16)
 
 

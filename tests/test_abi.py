@@ -1,0 +1,121 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+include/q2k.h declares, and rejects bad arguments with a status code before
+touching the GPU (the pages' `ensure!` checks before any launch:
+engram_v41/apply.rs `apply`, engram_v41.rs `rows_from_q2k`,
+moe_v41/init.rs `MoeV41::new`).  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q2k.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mmvq_q2_gb300 import build
+    build.build()
+    import mmvq_q2_gb300 as q
+    return q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*?[\s\*]+([a-z][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for want in ["q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16", "q2k_mmvq_q8_1", "q2k_mmvq_pair",
+                 "q2k_mmvq_experts", "dense_gemm_bf16", "swiglu_q8_1_rows", "q2k_moe_m1"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import mmvq_q2_gb300 as q
+    names = declared_functions()
+    assert sorted(q.EXPORTS) == names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_size_helpers(L):
+    assert L.q2k_row_bytes(256) == 84
+    assert L.q2k_row_bytes(16384) == 64 * 84
+    assert L.q2k_row_bytes(300) == 0 and L.q2k_row_bytes(0) == 0
+    assert L.q8_1_row_bytes(4096) == 128 * 36
+    assert L.q8_1_row_bytes(33) == 0
+    assert L.q2k_moe_m1_workspace_bytes(8, 4096, 2048) == 4608 + 2 * 8 * 2048 * 4 + 8 * 2304
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.q2k_status_string(s)
+    assert L.q2k_status_string(99) == b"unknown status"
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)      # never dereferenced: validation fails first
+ODD = P(0x10001)
+
+
+def test_gemv_validation(L):
+    assert L.q2k_gemv_bf16(None, 4, 256, FAKE, 1, 256, FAKE, 4, None) == 1
+    assert L.q2k_gemv_bf16(FAKE, 4, 300, FAKE, 1, 300, FAKE, 4, None) == 2   # K % 256
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, FAKE, 0, 256, FAKE, 4, None) == 2   # m = 0
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, FAKE, 9, 256, FAKE, 4, None) == 2   # m > 8
+    assert L.q2k_gemv_bf16(FAKE, 0, 256, FAKE, 1, 256, FAKE, 4, None) == 2   # N = 0
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, FAKE, 1, 128, FAKE, 4, None) == 2   # ldx < K
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, FAKE, 1, 256, FAKE, 3, None) == 2   # ldy < N
+    assert L.q2k_gemv_bf16(ODD, 4, 256, FAKE, 1, 256, FAKE, 4, None) == 3
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, ODD, 1, 256, FAKE, 4, None) == 3
+    assert L.q2k_gemv_bf16(FAKE, 4, 256, FAKE, 1, 256, P(0x10002), 4, None) == 3
+
+
+def test_mmvq_pair_experts_validation(L):
+    assert L.q2k_mmvq_q8_1(FAKE, 4, 512, None, 1, FAKE, 4, None) == 1
+    assert L.q2k_mmvq_q8_1(FAKE, 4, 512, FAKE, 9, FAKE, 4, None) == 2
+    assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 0, None) == 2
+    assert L.q2k_mmvq_pair(FAKE, 4, FAKE, None, 4, FAKE, 512, FAKE, 1, None) == 1
+    assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, -1, FAKE, 512, FAKE, 1, None) == 2
+    # experts: y_sum needs route weights; x_per_matrix is 0 or 1
+    assert L.q2k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, None, None, FAKE, None) == 1
+    assert L.q2k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, None, None, None, None) == 1
+    assert L.q2k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 2, FAKE, None, None, None) == 2
+    assert L.q2k_mmvq_experts(FAKE, 0, 64, 512, FAKE, 0, FAKE, None, None, None) == 2
+    assert L.q2k_mmvq_experts(P(0x10004), 8, 64, 512, FAKE, 0, FAKE, None, None, None) == 3
+
+
+def test_small_kernels_validation(L):
+    assert L.q2k_dequant_rows(None, 4, 256, None, 1, FAKE, None, None) == 1
+    assert L.q2k_dequant_rows(FAKE, 4, 200, None, 1, FAKE, None, None) == 2
+    assert L.q2k_dequant_rows(FAKE, 4, 256, None, 5, FAKE, None, None) == 2  # rows past the table
+    assert L.q2k_dequant_rows(FAKE, 4, 256, ODD, 2, FAKE, None, None) == 3
+    assert L.q8_1_quantize_rows(FAKE, 1, 48, 48, FAKE, None) == 2
+    assert L.q8_1_quantize_rows(FAKE, 1, 64, 32, FAKE, None) == 2
+    assert L.q8_1_quantize_rows(FAKE, 1, 64, 64, ODD, None) == 3
+    assert L.swiglu_q8_1_rows(FAKE, 1, 48, FAKE, None, None) == 2
+    assert L.swiglu_q8_1_rows(None, 1, 64, FAKE, None, None) == 1
+
+
+def test_moe_and_gemm_validation(L):
+    ws = L.q2k_moe_m1_workspace_bytes(2, 256, 256)
+    assert L.q2k_moe_m1(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, None, ws, None) == 6
+    assert L.q2k_moe_m1(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == 6
+    assert L.q2k_moe_m1(FAKE, 2, 300, 256, FAKE, FAKE, FAKE, FAKE, ws, None) == 2
+    assert L.q2k_moe_m1(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, P(0x10010), ws, None) == 3
+    assert L.dense_gemm_bf16(FAKE, 1, 12, 12, FAKE, 4, FAKE, 4, None) == 2
+    assert L.dense_gemm_bf16(P(0x10008), 1, 16, 16, FAKE, 4, FAKE, 4, None) == 3
+    assert L.dense_gemm_bf16(FAKE, 0, 16, 16, FAKE, 4, FAKE, 4, None) == 2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import mmvq_q2_gb300 as q
+    monkeypatch.setattr(q, "_lib", None)
+    monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        q.lib()

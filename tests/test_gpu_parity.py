@@ -1,0 +1,394 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars (from the method's statement of tolerances):
+  * dequantised bf16 rows and the row gather: bit-exact;
+  * q8_1 encoding: q, d and s bit-exact;
+  * bf16-activation projections: max|y - y_ref| / ||y_ref[t]||_2 <= 2e-3 per
+    token row;
+  * q8_1-activation projections: the same metric <= 1e-2 against the
+    projection of the original bf16 activations;
+  * dense GEMM: 2e-3 of each row's L2 norm.
+Full-size configurations are checked on sampled output rows the oracle can
+compute one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-3
+TOL_Q8 = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from mmvq_q2_gb300 import build
+    build.build()
+    import mmvq_q2_gb300 as q
+    q.lib()
+    yield q
+    torch.cuda.synchronize()
+    assert q.q2k_device_error(clear=True) == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bf16_dev(bits):
+    return dev(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def host_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rel_err_rows(y, ref):
+    y = np.atleast_2d(np.asarray(y, dtype=np.float64))
+    ref = np.atleast_2d(np.asarray(ref, dtype=np.float64))
+    return max(np.max(np.abs(y[t] - ref[t])) / max(np.linalg.norm(ref[t]), 1e-300) for t in range(ref.shape[0]))
+
+
+def x_f64(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ---- a1: gather + dequantise -------------------------------------------------
+
+def test_dequant_rows_contiguous_cfg0(lib):
+    W = synth.q2k_matrix(0, "cfg0.W", 512, 4096)
+    out = lib.q2k_dequant_rows(dev(W), 4096)
+    ref, bad = oracle.dequant_rows(W, 512, 4096, None, 512)
+    assert bad == 0
+    np.testing.assert_array_equal(host_bits(out), ref)
+
+
+def test_dequant_rows_gather_cfg1_bitexact_and_equal_to_contiguous_copy(lib):
+    n_table = 1 << 20
+    table = synth.q2k_blocks(0, "cfg1.table", n_table)
+    ids = synth.row_ids(0, "cfg1.ids", 16 * 8, n_table)
+    dt = dev(table)
+    out = lib.q2k_dequant_rows(dt, 256, ids=dev(ids))
+    ref, bad = oracle.dequant_rows(table, n_table, 256, ids, len(ids))
+    assert bad == 0
+    got = host_bits(out)
+    np.testing.assert_array_equal(got, ref)
+    copy = lib.q2k_dequant_rows(dev(table[ids]), 256)
+    np.testing.assert_array_equal(host_bits(copy), got)
+
+
+def test_dequant_rows_bad_ids_zero_rows_and_flag(lib):
+    table = synth.q2k_blocks(1, "bad.table", 64)
+    ids = np.array([3, -1, 64, 3, 63], dtype=np.int32)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = lib.q2k_dequant_rows(dev(table), 256, ids=dev(ids), err_flag=flag)
+    ref, bad = oracle.dequant_rows(table, 64, 256, ids, len(ids))
+    assert bad == 2 and flag.item() == 1
+    np.testing.assert_array_equal(host_bits(out), ref)
+    flag.zero_()
+    lib.q2k_dequant_rows(dev(table), 256, ids=dev(ids[[0, 4]]), err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+
+
+@pytest.mark.parametrize("K", [256, 512, 768, 1280])
+def test_dequant_rows_odd_widths_and_unaligned_output(lib, K):
+    W = synth.q2k_matrix(2, f"odd.{K}", 7, K)
+    full = torch.empty(7 * K + 1, dtype=torch.bfloat16, device="cuda")
+    out = full[1:].view(7, K)  # 2-byte aligned only
+    lib.q2k_dequant_rows(dev(W), K, out=out)
+    ref, _ = oracle.dequant_rows(W, 7, K, None, 7)
+    np.testing.assert_array_equal(host_bits(out.contiguous()), ref)
+
+
+# ---- a2: q8_1 ------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,K,pad", [(1, 32, 0), (3, 256, 8), (8, 4096, 0), (2, 16384, 32), (5, 2048, 0)])
+def test_q8_1_quantize_bitexact(lib, m, K, pad):
+    x = synth.bf16_normal(3, f"q8.{m}.{K}", (m, K + pad))
+    x[:, :32] = 0  # an all-zero block
+    xd = bf16_dev(x)[:, :K]
+    got = lib.q8_1_quantize_rows(xd).cpu().numpy()
+    ref = oracle.q8_1_quantize(np.ascontiguousarray(x[:, :K]))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_q8_1_ties_round_away_from_zero(lib):
+    vals = np.zeros((1, 64), dtype=np.float32)
+    vals[0, :8] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5]
+    x = synth.f32_to_bf16_bits(vals)
+    np.testing.assert_array_equal(lib.q8_1_quantize_rows(bf16_dev(x)).cpu().numpy(), oracle.q8_1_quantize(x))
+
+
+# ---- a3: Q2_K GEMV, bf16 activations -------------------------------------------
+
+SMALL = [(1, 256, 1), (5, 256, 8), (3, 512, 2), (7, 768, 3), (33, 1024, 4), (17, 2048, 5), (9, 4096, 8),
+         (130, 1280, 1), (1537, 2048, 1), (64, 4096, 6), (40, 8192, 7)]
+
+
+@pytest.mark.parametrize("N,K,m", SMALL)
+def test_gemv_bf16_small(lib, N, K, m):
+    W = synth.q2k_matrix(4, f"gemv.{N}.{K}", N, K)
+    x = synth.bf16_normal(4, f"gemv.x.{m}.{K}", (m, K))
+    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    ref = oracle.matvec(W, N, K, x_f64(x))
+    assert rel_err_rows(y, ref) <= TOL_BF16
+
+
+def test_gemv_bf16_unaligned_weights_take_the_copy_path(lib):
+    N, K = 21, 4096
+    W = synth.q2k_matrix(5, "unal", N, K)
+    buf = torch.zeros(W.size + 4, dtype=torch.uint8, device="cuda")
+    buf[4:] = dev(W.reshape(-1))
+    x = synth.bf16_normal(5, "unal.x", (2, K))
+    y = lib.q2k_gemv_bf16(buf[4:], bf16_dev(x)).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+
+
+def test_gemv_bf16_cfg0(lib):
+    W = synth.q2k_matrix(0, "cfg0.W", 512, 4096)
+    x = synth.bf16_normal(0, "cfg0.x", (1, 4096))
+    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, 512, 4096, x_f64(x))) <= TOL_BF16
+
+
+def test_gemv_bf16_output_stride_and_guard(lib):
+    N, K, m = 100, 1024, 3
+    W = synth.q2k_matrix(6, "guard", N, K)
+    x = synth.bf16_normal(6, "guard.x", (m, K))
+    buf = torch.full((m, N + 16), 7.0, dtype=torch.float32, device="cuda")
+    lib.q2k_gemv_bf16(dev(W), bf16_dev(x), out=buf[:, :N])
+    b = buf.cpu().numpy()
+    assert np.all(b[:, N:] == 7.0)
+    assert rel_err_rows(b[:, :N], oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+
+
+def test_gemv_bf16_extreme_activation_ranges(lib):
+    # groups with mixed magnitudes, tiny values and zeros
+    N, K = 16, 1024
+    W = synth.q2k_matrix(7, "ext", N, K)
+    v = np.random.default_rng(7).standard_normal((2, K)).astype(np.float32)
+    v[0, ::3] *= 1e-4
+    v[0, 5::7] = 0.0
+    v[1] *= 1e20
+    v[1, :64] = 0.0
+    x = synth.f32_to_bf16_bits(v)
+    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+
+
+@pytest.fixture(scope="module")
+def big_w():
+    W = synth.q2k_matrix(0, "sweep.W16384", 16384, 16384)
+    return W, dev(W)
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_gemv_bf16_16384_sampled(lib, big_w, m):
+    W, Wd = big_w
+    x = synth.bf16_normal(0, f"sweep.x{m}", (m, 16384))
+    y = lib.q2k_gemv_bf16(Wd, bf16_dev(x)).cpu().numpy()
+    rows = np.sort(np.random.default_rng(m).choice(16384, 48, replace=False))
+    rows[0], rows[-1] = 0, 16383
+    ref = oracle.matvec(np.ascontiguousarray(W[rows]), len(rows), 16384, x_f64(x))
+    assert rel_err_rows(y[:, rows], ref) <= TOL_BF16
+    assert np.all(np.isfinite(y))
+
+
+# ---- a4: Q2_K x q8_1 MMVQ -------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,m", SMALL)
+def test_mmvq_q8_1_small(lib, N, K, m):
+    W = synth.q2k_matrix(8, f"mmvq.{N}.{K}", N, K)
+    x = synth.bf16_normal(8, f"mmvq.x.{m}.{K}", (m, K))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q2k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
+    # diagnostic: against the exact projection of the values q8_1 encodes
+    assert rel_err_rows(y, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= 1e-4
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_mmvq_q8_1_16384_sampled(lib, big_w, m):
+    W, Wd = big_w
+    x = synth.bf16_normal(0, f"sweep.x{m}", (m, 16384))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    np.testing.assert_array_equal(xq.cpu().numpy(), oracle.q8_1_quantize(x))
+    y = lib.q2k_mmvq_q8_1(Wd, xq, 16384).cpu().numpy()
+    rows = np.sort(np.random.default_rng(10 + m).choice(16384, 48, replace=False))
+    ref = oracle.matvec(np.ascontiguousarray(W[rows]), len(rows), 16384, x_f64(x))
+    assert rel_err_rows(y[:, rows], ref) <= TOL_Q8
+
+
+# ---- a5: paired launch ------------------------------------------------------------
+
+@pytest.mark.parametrize("m", [1, 4, 8])
+def test_pair_cfg2_equals_two_singles_bitwise(lib, m):
+    K = 4096
+    Wa = synth.q2k_matrix(0, "cfg2.wq_a", 1024, K)
+    Wb = synth.q2k_matrix(0, "cfg2.wkv", 512, K)
+    x = synth.bf16_normal(0, f"cfg2.x{m}", (m, K))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    da, db = dev(Wa), dev(Wb)
+    ya, yb = lib.q2k_mmvq_pair(da, db, xq, K)
+    sa = lib.q2k_mmvq_q8_1(da, xq, K)
+    sb = lib.q2k_mmvq_q8_1(db, xq, K)
+    assert torch.equal(ya, sa) and torch.equal(yb, sb)
+    assert rel_err_rows(ya.cpu().numpy(), oracle.matvec(Wa, 1024, K, x_f64(x))) <= TOL_Q8
+    assert rel_err_rows(yb.cpu().numpy(), oracle.matvec(Wb, 512, K, x_f64(x))) <= TOL_Q8
+
+
+def test_pair_ragged_sizes(lib):
+    K = 768
+    Wa = synth.q2k_matrix(1, "pr.a", 37, K)
+    Wb = synth.q2k_matrix(1, "pr.b", 5, K)
+    x = synth.bf16_normal(1, "pr.x", (3, K))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    ya, yb = lib.q2k_mmvq_pair(dev(Wa), dev(Wb), xq, K)
+    assert torch.equal(ya, lib.q2k_mmvq_q8_1(dev(Wa), xq, K))
+    assert torch.equal(yb, lib.q2k_mmvq_q8_1(dev(Wb), xq, K))
+
+
+# ---- a6: routed experts -------------------------------------------------------------
+
+@pytest.mark.parametrize("per_matrix", [False, True])
+def test_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
+    n_mat, N, K = 5, 300, 512
+    mats = [dev(synth.q2k_matrix(2, f"ex.{e}", N, K)) for e in range(n_mat)]
+    rows = n_mat if per_matrix else 1
+    x = synth.bf16_normal(2, f"ex.x{rows}", (rows, K))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    w = np.float32([0.1, 0.3, 0.05, 0.25, 0.3])
+    wt = dev(w)
+    tbl = lib.pointer_table(mats)
+    ysum = torch.empty(N, dtype=torch.float32, device="cuda")
+    y, _ = lib.q2k_mmvq_experts(tbl, N, K, xq, x_per_matrix=per_matrix, route_w=wt, y_sum=ysum)
+    for e in range(n_mat):
+        xe = xq[e:e + 1] if per_matrix else xq
+        assert torch.equal(y[e:e + 1], lib.q2k_mmvq_q8_1(mats[e], xe, K)), e
+    yh = y.cpu().numpy().astype(np.float64)
+    ref = (w.astype(np.float64)[:, None] * yh).sum(0)
+    assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
+    # only the sum
+    ys2 = torch.empty(N, dtype=torch.float32, device="cuda")
+    lib.q2k_mmvq_experts(tbl, N, K, xq, x_per_matrix=per_matrix, route_w=wt, y_sum=ys2, want_y=False)
+    assert torch.equal(ys2, ysum)
+
+
+def test_swiglu_q8_1_against_oracle(lib):
+    E, N = 3, 2048
+    g = np.random.default_rng(3).standard_normal((2 * E, N)).astype(np.float32) * 2
+    gu = dev(g)
+    h16 = torch.empty((E, N), dtype=torch.bfloat16, device="cuda")
+    hq, _ = lib.swiglu_q8_1_rows(gu, h_bf16=h16)
+    got16 = host_bits(h16)
+    gb = x_f64(oracle.round_bf16(g[:E].astype(np.float64)))
+    ub = x_f64(oracle.round_bf16(g[E:].astype(np.float64)))
+    ref16 = oracle.round_bf16(oracle.swiglu(gb, ub))
+    # silu in fp32 vs fp64: at most one bf16 step apart
+    diff = np.abs(got16.astype(np.int32) - ref16.astype(np.int32))
+    same_sign = (got16 >> 15) == (ref16 >> 15)
+    assert np.all((diff <= 1) & same_sign | (got16 == ref16))
+    np.testing.assert_array_equal(hq.cpu().numpy(), oracle.q8_1_quantize(got16))
+
+
+@pytest.fixture(scope="module")
+def cfg3():
+    E_all, topk, dim, inter = 256, 8, 4096, 2048
+    mats = {}
+    dev_mats = {}
+    for e in range(E_all):
+        for kind, shape in (("gate", (inter, dim)), ("up", (inter, dim)), ("down", (dim, inter))):
+            a = synth.q2k_matrix(0, f"cfg3.{kind}{e}", *shape)
+            dev_mats[(kind, e)] = dev(a)
+            mats[(kind, e)] = a
+    ids, w = synth.expert_route(0, E_all, topk)
+    x = synth.bf16_normal(0, "cfg3.x", (1, dim))
+    return dict(mats=mats, dev=dev_mats, ids=ids, w=w, x=x, dim=dim, inter=inter, topk=topk)
+
+
+def test_moe_m1_cfg3(lib, cfg3):
+    c = cfg3
+    ids, w = c["ids"], c["w"]
+    ptrs = [c["dev"][("gate", int(e))] for e in ids] + [c["dev"][("up", int(e))] for e in ids] + \
+           [c["dev"][("down", int(e))] for e in ids]
+    tbl = lib.pointer_table(ptrs)
+    y, ws = lib.q2k_moe_m1(tbl, len(ids), c["dim"], c["inter"], bf16_dev(c["x"][0]), dev(w))
+    y = y.cpu().numpy()
+    gate = [c["mats"][("gate", int(e))] for e in ids]
+    up = [c["mats"][("up", int(e))] for e in ids]
+    down = [c["mats"][("down", int(e))] for e in ids]
+    ref = oracle.moe_m1(c["x"], gate, up, down, w, c["dim"], c["inter"])
+    assert rel_err_rows(y, ref["y"]) <= TOL_Q8
+    refq = oracle.moe_m1(c["x"], gate, up, down, w, c["dim"], c["inter"], quantized=True)
+    assert rel_err_rows(y, refq["y"]) <= 2e-3
+    # the chain equals its steps run one by one
+    xq = lib.q8_1_quantize_rows(bf16_dev(c["x"]))
+    gu, _ = lib.q2k_mmvq_experts(lib.pointer_table(ptrs[:16]), c["inter"], c["dim"], xq)
+    hq, _ = lib.swiglu_q8_1_rows(gu)
+    ys = torch.empty(c["dim"], dtype=torch.float32, device="cuda")
+    lib.q2k_mmvq_experts(lib.pointer_table(ptrs[16:]), c["dim"], c["inter"], hq, x_per_matrix=True,
+                         route_w=dev(w), y_sum=ys, want_y=False)
+    np.testing.assert_array_equal(ys.cpu().numpy(), y)
+
+
+# ---- a7: dense GEMM -----------------------------------------------------------------
+
+@pytest.mark.parametrize("m,N,K", [(1, 8, 16), (3, 65, 64), (16, 130, 200), (17, 64, 1024), (64, 256, 512),
+                                   (100, 70, 136), (256, 128, 256)])
+def test_dense_gemm_small(lib, m, N, K):
+    x = synth.bf16_normal(9, f"dg.x.{m}.{K}", (m, K))
+    W = synth.bf16_normal(9, f"dg.w.{N}.{K}", (N, K), std=0.02)
+    y = lib.dense_gemm_bf16(bf16_dev(x), bf16_dev(W)).cpu().numpy()
+    assert rel_err_rows(y, oracle.dense_gemm(x, W)) <= TOL_BF16
+
+
+def test_engram_cfg1_rows_then_gemm(lib):
+    n_table, T, cols, N = 1 << 20, 16, 8, 4096 * 5
+    table = synth.q2k_blocks(0, "cfg1.table", n_table)
+    ids = synth.row_ids(0, "cfg1.ids", T * cols, n_table)
+    wkv = synth.bf16_normal(0, "cfg1.wkv", (N, cols * 256), std=0.02)
+    rows = lib.q2k_dequant_rows(dev(table), 256, ids=dev(ids))
+    y = lib.dense_gemm_bf16(rows.view(T, cols * 256), bf16_dev(wkv)).cpu().numpy()
+    ref_rows, ref_y = oracle.engram_rows_projection(table, n_table, ids, T, cols, wkv)
+    np.testing.assert_array_equal(host_bits(rows), ref_rows)
+    assert rel_err_rows(y, ref_y) <= TOL_BF16
+
+
+@pytest.mark.parametrize("m", [64, 256])
+def test_dense_gemm_16384_sampled(lib, m):
+    N = K = 16384
+    W = synth.bf16_normal(0, "sweep.dense.W", (N, K), std=0.02)
+    x = synth.bf16_normal(0, f"sweep.dense.x{m}", (m, K))
+    y = lib.dense_gemm_bf16(bf16_dev(x), bf16_dev(W)).cpu().numpy()
+    rows = np.sort(np.random.default_rng(m).choice(N, 16, replace=False))
+    ref = oracle.dense_gemm(x, np.ascontiguousarray(W[rows]))
+    assert rel_err_rows(y[:, rows], ref) <= TOL_BF16
+
+
+def test_q2k_gemv_matches_dense_gemm_over_the_expansion(lib):
+    # engram_v41.rs `wkv_q2k`: the Q2_K GEMV and the bf16 GEMV over its bf16
+    # expansion agree (bit for bit on the page's kernels; here within 2e-3,
+    # the two kernels reduce in different orders and the expansion rounds
+    # weights to bf16).
+    N, K = 512, 4096
+    W = synth.q2k_matrix(0, "cfg0.W", N, K)
+    x = synth.bf16_normal(0, "cfg0.x", (1, K))
+    Wd = dev(W)
+    y_q = lib.q2k_gemv_bf16(Wd, bf16_dev(x)).cpu().numpy()
+    W16 = lib.q2k_dequant_rows(Wd, K)
+    y_d = lib.dense_gemm_bf16(bf16_dev(x), W16).cpu().numpy()
+    assert rel_err_rows(y_q, y_d) <= TOL_BF16
+
+
+def test_repeat_calls_are_bitwise_identical(lib, big_w):
+    _, Wd = big_w
+    x = bf16_dev(synth.bf16_normal(0, "sweep.x1", (1, 16384)))
+    a = lib.q2k_gemv_bf16(Wd, x)
+    b = lib.q2k_gemv_bf16(Wd, x)
+    assert torch.equal(a, b)
