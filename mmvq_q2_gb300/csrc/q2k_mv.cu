@@ -5,26 +5,30 @@
 // q8_1 input, one launch) and moe_v41/init.rs (`kquant_mmvq_q2_k_experts_w8`
 // batches, `moe_v41_accumulate` route-weighted sum).
 //
-// Design (GB300):
-//  * Weight rows stream into a ring of shared-memory stages with 1-D bulk
-//    asynchronous copies (cp.async.bulk, the TMA engine) signalled on
-//    mbarriers.  Lane 0 of warp 0 issues them: the ring is primed up front
-//    and each slot is refilled once every warp has released it (one
-//    mbarrier arrival per warp).  Rows that are not 16-byte aligned are
-//    copied by warp 0's lanes instead.  Every wait is bounded.
-//  * Each consumer thread owns a fixed K-slice of every row (SW words of a
-//    block's qs, i.e. 16*SW weights spread over 4 sub-blocks) and keeps the
-//    matching activations in registers for all rows it visits, so the only
-//    per-row traffic is the weight stream itself.
+// Design (GB300, one CTA of 16 warps per SM):
+//  * Weight rows stream into a ring of ~40 KB shared-memory stages with 1-D
+//    bulk asynchronous copies (cp.async.bulk, the TMA engine) signalled on
+//    mbarriers.  Warp 0 primes the ring; afterwards the last warp to finish
+//    with a slot (a shared-memory counter) refills it, so no warp ever
+//    blocks to produce.  Rows that are not 16-byte aligned are copied with
+//    4-byte loads instead.  Every wait is bounded.
+//  * The activations of the CTA's K chunk are staged once in shared memory;
+//    each thread then owns a fixed K-slice of every row (SW words of a
+//    block's qs: 16*SW weights over 4 sub-blocks) and keeps the matching
+//    activations in registers for all rows it visits, so the only per-row
+//    traffic is the weight stream itself.
 //  * Codes are extracted four at a time with one AND per register (the code
 //    of pair j stays at bit 2j of each byte, i.e. scaled by 4^j; the 4^-j is
-//    folded into the per-sub-block activation scale) and multiplied by
-//    DP4A (q8_1 activations) or two DP2A (bf16 activations as 16-bit fixed
-//    point with one exponent per group).
-//  * Per sub-block: y += d*sc*xscale*S - dmin*m*sum(x), with the scale and
-//    min nibbles converted to float once per sub-block and shared by all
-//    tokens.  Row partial sums are reduced with warp shuffles and, when a
-//    row spans several warps, through shared memory in a fixed order.
+//    folded into the activation scale) and multiplied by DP4A (q8_1
+//    activations) or two DP2A (bf16 activations as 16-bit fixed point with
+//    one exponent per group of 16).
+//  * Per sub-block: y += d*sc*xscale*S - dmin*m*sum(x).  S*sc is formed in
+//    int32; the min term is a dot product of the min nibbles with the
+//    group sums (16-bit fixed point, one exponent per slice).
+//  * Partial sums: a transpose-reduce across each warp's lanes deposits one
+//    (row, token) sum per warp in shared memory; after the stage loop the
+//    warps' sums are added in a fixed order (deterministic), which also
+//    fuses the experts' route-weighted sum.
 #include "q2k_common.cuh"
 #include "q2k_internal.h"
 
@@ -34,21 +38,26 @@ namespace q2k {
 
 __device__ int g_mv_error = 0;
 
-// Row slots per thread per stage: fewer for more tokens (registers).
-__host__ __device__ constexpr int rpt_max(int m) { return m <= 2 ? 4 : (m <= 4 ? 2 : 1); }
+constexpr int kThreads = 512;  // one CTA of 16 warps per SM
+
+// Rows per thread per reduction unit (fewer for more tokens: registers).
+__host__ __device__ constexpr int rpt_for(int m) { return m <= 2 ? 4 : (m <= 4 ? 2 : 1); }
+__host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
+__host__ __device__ constexpr int log2_exact(int v) { return v <= 1 ? 0 : 1 + log2_exact(v / 2); }
 
 struct MvArgs {
     int n_seg;
     int table;  // 1: W_table segments, stacked over one row range
     const void* const* W_table;
     const uint8_t* W[2];
-    int64_t N[2];
+    int N[2];
     int64_t row_bytes;  // bytes of a full weight row
     int kb0;            // first block column of this K chunk
     int nbc;            // blocks in this K chunk
     const uint8_t* x;
     int64_t x_tok_stride;
     int64_t x_seg_stride;
+    int x_align;  // 16, 4 or 2: widest copy the activation addresses allow
     float* y[2];
     int64_t ldy[2];
     float* y_exp;
@@ -56,71 +65,72 @@ struct MvArgs {
     float* y_sum;
     int accumulate;
     // decomposition
-    int rpt;         // row slots per thread per stage (<= rpt_max(M))
-    int s_real;      // slices per row
-    int s_pad;       // lanes per row group
-    int groups;      // row groups
-    int tc;          // consumer threads
-    int rps;         // rows per stage (multiple of groups)
-    int nst;         // stages in the ring
+    int s_real;         // slices per row
+    int s_pad;          // lanes per row group
+    int groups;         // row groups
+    int tc;             // threads
+    int sub;            // reduction units per stage
+    int rps;            // rows per stage = groups * RPT * sub
+    int nst;            // stages in the ring
+    int rows_total;     // concat: N0 + N1; table: N
+    int max_stages;     // stages of the largest CTA
     uint32_t rstride;   // shared-memory row stride (16-byte multiple)
     uint32_t stage_bytes;
-    int64_t rows_total;  // concat: N0 + N1; table: N
-    int ysum_cap;
+    // shared-memory layout (byte offsets, each 16-byte aligned)
+    uint32_t off_x, off_bar, off_tab, off_cnt, off_red;
 };
 
 struct Stage {
     int e;
-    int64_t row0;
+    int row0;
     int nrows;
 };
 
-// Rows [lo, hi) of this CTA.
-__device__ __forceinline__ void cta_range(const MvArgs& a, int64_t& lo, int64_t& hi)
-{
-    lo = (a.rows_total * (int64_t)blockIdx.x) / gridDim.x;
-    hi = (a.rows_total * (int64_t)(blockIdx.x + 1)) / gridDim.x;
-}
+// Walks this CTA's stages: rows [lo, hi) of the row space, split at segment
+// ends (concat) or repeated for every segment (table).
+struct StageIter {
+    int e, r, end, lo, hi;
+    __device__ __forceinline__ void init(const MvArgs& a, int lo_, int hi_)
+    {
+        lo = lo_;
+        hi = hi_;
+        if (a.table || lo < a.N[0]) {
+            e = 0;
+            r = lo;
+            end = a.table ? hi : min(hi, a.N[0]);
+        } else {
+            e = 1;
+            r = lo - a.N[0];
+            end = hi - a.N[0];
+        }
+    }
+    __device__ __forceinline__ Stage get(const MvArgs& a) const { return Stage{e, r, min(a.rps, end - r)}; }
+    __device__ __forceinline__ void next(const MvArgs& a)
+    {
+        r += a.rps;
+        if (r < end)
+            return;
+        if (a.table) {
+            ++e;
+            r = lo;
+        } else if (e == 0 && hi > a.N[0]) {
+            e = 1;
+            r = max(lo, a.N[0]) - a.N[0];
+            end = hi - a.N[0];
+        }
+    }
+};
 
-__device__ __forceinline__ int stage_count(const MvArgs& a, int64_t lo, int64_t hi)
+__device__ __forceinline__ int stage_count(const MvArgs& a, int lo, int hi)
 {
     if (hi <= lo)
         return 0;
-    if (a.table) {
-        int per = (int)((hi - lo + a.rps - 1) / a.rps);
-        return per * a.n_seg;
-    }
-    int64_t n0 = a.N[0];
-    int64_t l0 = max((int64_t)0, min(hi, n0) - lo);
-    int64_t l1 = max((int64_t)0, hi - max(lo, n0));
-    return (int)((l0 + a.rps - 1) / a.rps + (l1 + a.rps - 1) / a.rps);
-}
-
-__device__ __forceinline__ Stage stage_at(const MvArgs& a, int64_t lo, int64_t hi, int i)
-{
-    Stage s;
-    if (a.table) {
-        int per = (int)((hi - lo + a.rps - 1) / a.rps);
-        s.e = i / per;
-        int c = i - s.e * per;
-        s.row0 = lo + (int64_t)c * a.rps;
-        s.nrows = (int)min((int64_t)a.rps, hi - s.row0);
-        return s;
-    }
-    int64_t n0 = a.N[0];
-    int64_t b0 = lo, e0 = min(hi, n0);
-    int c0 = e0 > b0 ? (int)((e0 - b0 + a.rps - 1) / a.rps) : 0;
-    if (i < c0) {
-        s.e = 0;
-        s.row0 = b0 + (int64_t)i * a.rps;
-        s.nrows = (int)min((int64_t)a.rps, e0 - s.row0);
-    } else {
-        int64_t b1 = max(lo, n0);
-        s.e = 1;
-        s.row0 = (b1 - n0) + (int64_t)(i - c0) * a.rps;
-        s.nrows = (int)min((int64_t)a.rps, (hi - n0) - s.row0);
-    }
-    return s;
+    if (a.table)
+        return ((hi - lo + a.rps - 1) / a.rps) * a.n_seg;
+    const int n0 = a.N[0];
+    const int l0 = max(0, min(hi, n0) - lo);
+    const int l1 = max(0, hi - max(lo, n0));
+    return (l0 + a.rps - 1) / a.rps + (l1 + a.rps - 1) / a.rps;
 }
 
 __device__ __forceinline__ const uint8_t* seg_weights(const MvArgs& a, int e)
@@ -141,44 +151,113 @@ struct Slice {
     static constexpr int NH = (SW == 8) ? 2 : 1;           // sub-block halves covered
     static constexpr int WPH = SW / NH;                    // qs words per half
     uint32_t xa[M][4][SW][NA];
-    float xp[M][4][NH];
-    float xs[M][4][NH];
+    float xp[M][4][NH];       // scale of the integer sum of pair j (includes 4^-j)
+    uint32_t xs16[M][NH][2];  // group sums (j = 0,1 | 2,3) as 16-bit fixed point
+    float xsb[M][NH];         // their common power-of-two scale
 };
 
-// Load and convert this thread's activation slice.  Slice geometry: block
-// column bcol (absolute), half n, first qs word wi0 (0..7) within the half.
-// Weight of (j, word w, byte i) is k = bcol*256 + 128n + 32j + 4w + i.
+// Pack the four group sums of one (token, half) as 16-bit fixed point with
+// a common power-of-two exponent (error below 2^-15 of the largest).
 template <int M, int ACT, int SW>
-__device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t* xseg, int64_t tok_stride,
-                                           int bcol, int n, int wi0, bool active)
+__device__ __forceinline__ void pack_sums(Slice<M, ACT, SW>& sl, int t, int hh, const float (&xs)[4])
+{
+    const float amax = fmaxf(fmaxf(fabsf(xs[0]), fabsf(xs[1])), fmaxf(fabsf(xs[2]), fabsf(xs[3])));
+    const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;
+    if (eb < 27u) {
+        sl.xs16[t][hh][0] = sl.xs16[t][hh][1] = 0u;
+        sl.xsb[t][hh] = 0.f;
+        return;
+    }
+    const float scale = __uint_as_float((268u - eb) << 23);  // |xs * scale| < 2^15
+    int q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        q[j] = __float2int_rn(xs[j] * scale);
+    sl.xs16[t][hh][0] = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[1] << 16);
+    sl.xs16[t][hh][1] = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
+    sl.xsb[t][hh] = __uint_as_float((eb - 14u) << 23);
+}
+
+// Bytes of one token's activations per block column in the shared staging
+// region: 256 bf16 values, or 8 q8_1 blocks.
+template <int ACT>
+__host__ __device__ constexpr int x_bytes_per_block() { return ACT == ACT_BF16 ? 512 : 8 * kQ8Bytes; }
+
+// Copy the K chunk of every token's activations for one segment into shared
+// memory (all threads of the CTA; coalesced, 16-byte pieces when aligned).
+template <int M, int ACT>
+__device__ __forceinline__ void stage_x(const uint8_t* xseg, int64_t tok_stride, int kb0, int nbc, int align,
+                                        uint8_t* xsm)
+{
+    const int rowb = nbc * x_bytes_per_block<ACT>();
+    const uint8_t* src0 = xseg + (int64_t)kb0 * x_bytes_per_block<ACT>();
+    for (int t = 0; t < M; ++t) {
+        const uint8_t* src = src0 + t * tok_stride;
+        uint8_t* dst = xsm + t * rowb;
+        if (align >= 16) {
+            for (int o = threadIdx.x * 16; o < rowb; o += blockDim.x * 16)
+                *reinterpret_cast<uint4*>(dst + o) = __ldg(reinterpret_cast<const uint4*>(src + o));
+        } else if (align >= 4) {
+            for (int o = threadIdx.x * 4; o < rowb; o += blockDim.x * 4)
+                *reinterpret_cast<uint32_t*>(dst + o) = ldg32_nc(src + o);
+        } else {
+            for (int o = threadIdx.x * 2; o < rowb; o += blockDim.x * 2)
+                *reinterpret_cast<uint16_t*>(dst + o) = *reinterpret_cast<const uint16_t*>(src + o);
+        }
+    }
+}
+
+// Build this thread's activation slice from the staged K chunk.  Slice
+// geometry: block b within the chunk, half n, first qs word wi0 (0..7).
+// Weight of (j, word w, byte i) is k = b*256 + 128n + 32j + 4w + i.
+template <int M, int ACT, int SW>
+__device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t* xsm, int nbc, int b, int n, int wi0,
+                                           bool active)
 {
     using S = Slice<M, ACT, SW>;
+    const int rowb = nbc * x_bytes_per_block<ACT>();
 #pragma unroll
     for (int t = 0; t < M; ++t) {
-        const uint8_t* xt = xseg + t * tok_stride;
+        const uint8_t* xt = xsm + t * rowb;
+        float xsum[S::NH][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if constexpr (ACT == ACT_BF16) {
-                const uint16_t* xv = reinterpret_cast<const uint16_t*>(xt);
 #pragma unroll
                 for (int hh = 0; hh < S::NH; ++hh) {
+                    // S::WPH*4 consecutive bf16 values, 8*WPH bytes, aligned to 8*WPH
+                    uint32_t raw[S::WPH * 2];
+                    const uint8_t* p = xt + 2 * (b * 256 + 128 * n + 32 * j + 4 * (wi0 + hh * S::WPH));
+                    if constexpr (S::WPH >= 2) {
+#pragma unroll
+                        for (int q = 0; q < S::WPH / 2; ++q) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * q);
+                            raw[4 * q] = u.x;
+                            raw[4 * q + 1] = u.y;
+                            raw[4 * q + 2] = u.z;
+                            raw[4 * q + 3] = u.w;
+                        }
+                    } else {
+                        const uint2 u = *reinterpret_cast<const uint2*>(p);
+                        raw[0] = u.x;
+                        raw[1] = u.y;
+                    }
                     float v[S::WPH * 4];
                     float amax = 0.f;
 #pragma unroll
-                    for (int wl = 0; wl < S::WPH; ++wl)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            int64_t k = (int64_t)bcol * 256 + 128 * n + 32 * j + 4 * (wi0 + hh * S::WPH + wl) + i;
-                            float f = active ? bf16_bits_f(xv[k]) : 0.f;
-                            v[wl * 4 + i] = f;
-                            amax = fmaxf(amax, fabsf(f));
-                        }
-                    uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;  // biased exponent of amax
+                    for (int q = 0; q < S::WPH * 2; ++q) {
+                        const float lo = active ? __uint_as_float(raw[q] << 16) : 0.f;
+                        const float hi = active ? __uint_as_float(raw[q] & 0xFFFF0000u) : 0.f;
+                        v[2 * q] = lo;
+                        v[2 * q + 1] = hi;
+                        amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                    }
+                    const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;  // biased exponent of amax
                     int sum = 0;
                     if (eb >= 27u) {
                         // x16 = x * 2^(141-eb): |x16| < 2^15, exact for the group's
                         // largest 2^8 range; xp = 2^(eb-141) * 4^-j.
-                        float scale = __uint_as_float((268u - eb) << 23);
+                        const float scale = __uint_as_float((268u - eb) << 23);
 #pragma unroll
                         for (int wl = 0; wl < S::WPH; ++wl) {
                             int q[4];
@@ -191,7 +270,7 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
                             sl.xa[t][j][hh * S::WPH + wl][1] = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
                         }
                         sl.xp[t][j][hh] = __uint_as_float((eb - 14u - 2u * j) << 23);
-                        sl.xs[t][j][hh] = (float)sum * __uint_as_float((eb - 14u) << 23);
+                        xsum[hh][j] = (float)sum * __uint_as_float((eb - 14u) << 23);
                     } else {
 #pragma unroll
                         for (int wl = 0; wl < S::WPH; ++wl) {
@@ -199,28 +278,31 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
                             sl.xa[t][j][hh * S::WPH + wl][1] = 0u;
                         }
                         sl.xp[t][j][hh] = 0.f;
-                        sl.xs[t][j][hh] = 0.f;
+                        xsum[hh][j] = 0.f;
                     }
                 }
             } else {
-                // q8_1 block (bcol*8 + 4n + j): fp16 d at +0, q[32] at +4.
-                const uint8_t* qb = xt + ((int64_t)bcol * 8 + 4 * n + j) * kQ8Bytes;
-                float d = active ? half_lo_f(ldg32_nc(qb)) : 0.f;
+                // q8_1 block (b*8 + 4n + j) of the chunk: fp16 d at +0, q[32] at +4.
+                const uint8_t* qb = xt + (b * 8 + 4 * n + j) * kQ8Bytes;
+                const float d = active ? half_lo_f(lds32(qb)) : 0.f;
 #pragma unroll
                 for (int hh = 0; hh < S::NH; ++hh) {
                     int sum = 0;
 #pragma unroll
                     for (int wl = 0; wl < S::WPH; ++wl) {
-                        int w = wi0 + hh * S::WPH + wl;
-                        uint32_t qv = active ? ldg32_nc(qb + 4 + 4 * w) : 0u;
+                        const int w = wi0 + hh * S::WPH + wl;
+                        const uint32_t qv = active ? lds32(qb + 4 + 4 * w) : 0u;
                         sl.xa[t][j][hh * S::WPH + wl][0] = qv;
                         sum = dp4a_us(0x01010101u, qv, sum);
                     }
                     sl.xp[t][j][hh] = d * __uint_as_float((127u - 2u * j) << 23);
-                    sl.xs[t][j][hh] = d * (float)sum;
+                    xsum[hh][j] = d * (float)sum;
                 }
             }
         }
+#pragma unroll
+        for (int hh = 0; hh < S::NH; ++hh)
+            pack_sums<M, ACT, SW>(sl, t, hh, xsum[hh]);
     }
 }
 
@@ -247,13 +329,16 @@ __device__ __forceinline__ void slice_dot(const Slice<M, ACT, SW>& sl, const uin
         const uint32_t sb = __byte_perm(s0, s1, h | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12));
         const uint32_t scn = sb & 0x0F0F0F0Fu;
         const uint32_t mnn = (sb >> 4) & 0x0F0F0F0Fu;
-        const float sc[4] = {byte_as_float<0>(scn), byte_as_float<1>(scn), byte_as_float<2>(scn),
-                             byte_as_float<3>(scn)};
-        const float mn[4] = {byte_as_float<0>(mnn), byte_as_float<1>(mnn), byte_as_float<2>(mnn),
-                             byte_as_float<3>(mnn)};
+        // scale nibbles as integers: the sub-block sum is scaled in int32
+        // (|S| * 15 < 2^31) before its one conversion to float
+        const int sci[4] = {(int)__byte_perm(scn, 0u, 0x4440u), (int)__byte_perm(scn, 0u, 0x4441u),
+                            (int)__byte_perm(scn, 0u, 0x4442u), (int)__byte_perm(scn, 0u, 0x4443u)};
 #pragma unroll
         for (int t = 0; t < M; ++t) {
-            float A = 0.f, B = 0.f;
+            // min term: sum_j m_j * xsum_j as two 16x8-bit dot products
+            const int Bi = dp2a_hi_su(sl.xs16[t][hh][1], mnn, dp2a_lo_su(sl.xs16[t][hh][0], mnn, 0));
+            const float B = sl.xsb[t][hh] * (float)Bi;
+            float A = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 int Sacc = 0;
@@ -268,8 +353,7 @@ __device__ __forceinline__ void slice_dot(const Slice<M, ACT, SW>& sl, const uin
                         Sacc = dp4a_us(c, sl.xa[t][j][w][0], Sacc);
                     }
                 }
-                A = fmaf(sc[j], sl.xp[t][j][hh] * (float)Sacc, A);
-                B = fmaf(mn[j], sl.xs[t][j][hh], B);
+                A = fmaf(sl.xp[t][j][hh], (float)(Sacc * sci[j]), A);
             }
             acc[t] = fmaf(d, A, fmaf(-dmin, B, acc[t]));
         }
@@ -282,67 +366,107 @@ __device__ __forceinline__ void flag_error(volatile int* abort_flag)
     *abort_flag = 1;
 }
 
-template <int M, int ACT, int SW, int MAXT, int MINB>
-__global__ void __launch_bounds__(MAXT, MINB) q2k_mv_kernel(const MvArgs a)
+// Sum VP values over the 32 lanes of a warp: after the exchanges each lane
+// holds the full sum of value index lane >> (5 - log2 VP).
+template <int VP>
+__device__ __forceinline__ float transpose_reduce(float (&v)[VP], int lane)
+{
+#pragma unroll
+    for (int n = VP / 2, o = 16; n >= 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = up ? v[i] : v[i + n];
+            const float keep = up ? v[i + n] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 >> log2_exact(VP); o >= 1; o >>= 1)
+        r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+// All lanes wait on the barrier (no divergence); the warp proceeds only if
+// every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane)
+{
+    const bool ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait_bounded(bar, parity, abort_flag));
+    if (!ok && lane == 0)
+        flag_error(abort_flag);
+    return ok;
+}
+
+template <int M, int ACT, int SW>
+__global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     using S = Slice<M, ACT, SW>;
     constexpr int SPB = 16 / SW;  // slices per block
-    constexpr int RPT = rpt_max(M);
-
-    // shared layout: [stages][ mbarriers full/empty, abort ][ reduction x2 ][ ysum ]
-    uint8_t* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)a.nst * a.stage_bytes);
-    const int wpg = a.s_pad >= 32 ? a.s_pad / 32 : 1;  // warps per row group
-    float* red = reinterpret_cast<float*>(bars + 2 * a.nst + 2);
-    const int red_one = a.groups * RPT * M * wpg;
-    float* ysum = red + 2 * red_one;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * a.nst);
+    constexpr int RPT = rpt_for(M);
+    constexpr int V = RPT * M;        // partial sums per thread per unit
+    constexpr int VP = pow2_ceil(V);  // padded to a power of two (<= 32)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = a.tc >> 5;
+    const int wpg = a.s_pad >= 32 ? a.s_pad / 32 : 1;  // warps per row group
+    const int red_one = a.groups * wpg * VP;           // floats per reduction unit
+    const int unit_rows = a.groups * RPT;              // rows of one reduction unit
 
-    int64_t lo, hi;
-    cta_range(a, lo, hi);
+    // shared layout (offsets from the host, 16-byte aligned): weight ring |
+    // staged activations | full barriers, abort flag | stage table |
+    // release counters, copies issued | partial sums of every unit
+    uint8_t* ring = smem;
+    uint8_t* xsm = smem + a.off_x;
+    uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full_b + a.nst);
+    int4* tab = reinterpret_cast<int4*>(smem + a.off_tab);  // {e, row0, nrows, -} per stage
+    int* cnt = reinterpret_cast<int*>(smem + a.off_cnt);    // warps done with each slot
+    int* n_issued = cnt + a.nst;
+    float* red = reinterpret_cast<float*>(smem + a.off_red);
+
+    const int lo = (int)(((int64_t)a.rows_total * blockIdx.x) / gridDim.x);
+    const int hi = (int)(((int64_t)a.rows_total * (blockIdx.x + 1)) / gridDim.x);
     const int nstages = stage_count(a, lo, hi);
 
     if (tid == 0) {
-        for (int s = 0; s < a.nst; ++s) {
-            mbar_init(smem_u32(&bars[s]), 1);
-            mbar_init(smem_u32(&bars[a.nst + s]), nwarps);
-        }
+        for (int s = 0; s < a.nst; ++s)
+            mbar_init(smem_u32(&full_b[s]), 1);
         *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (a.table && a.y_sum) {
-        for (int r = tid; r < a.ysum_cap; r += blockDim.x) {
-            int64_t row = lo + r;
-            ysum[r] = (a.accumulate && row < hi) ? a.y_sum[row] : 0.f;
+        StageIter it;
+        it.init(a, lo, hi);
+        for (int i = 0; i < nstages; ++i) {
+            const Stage st = it.get(a);
+            tab[i] = make_int4(st.e, st.row0, st.nrows, 0);
+            it.next(a);
         }
+        for (int s = 0; s <= a.nst; ++s)
+            cnt[s] = 0;
+        fence_mbar_init();
     }
     __syncthreads();
 
-    // Producer role (warp 0): fill stage i into its ring slot.  Bulk copies
-    // when every row start and length is 16-byte aligned, else warp-wide
-    // 4-byte copies.  Called by all lanes of warp 0.
+    // ---- producer role: stage i into slot i % nst.  Bulk copies are issued
+    // by lane 0; the 4-byte fallback uses the whole warp. ----
     const uint32_t chunk = (uint32_t)a.nbc * kBlockBytes;
     auto produce = [&](int i) {
         const int slot = i % a.nst;
-        const Stage st = stage_at(a, lo, hi, i);
-        const uint8_t* src0 = seg_weights(a, st.e) + st.row0 * a.row_bytes + (int64_t)a.kb0 * kBlockBytes;
+        const int4 st = tab[i];
+        const uint8_t* src0 = seg_weights(a, st.x) + (int64_t)st.y * a.row_bytes + (int64_t)a.kb0 * kBlockBytes;
         uint8_t* dst0 = ring + (size_t)slot * a.stage_bytes;
-        const uint32_t full = smem_u32(&bars[slot]);
+        const uint32_t fb = smem_u32(&full_b[slot]);
         const bool tma = ((reinterpret_cast<uintptr_t>(src0) | (uintptr_t)a.row_bytes | chunk) & 15u) == 0;
         if (tma) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(full, chunk * st.nrows);
-                for (int r = 0; r < st.nrows; ++r)
-                    bulk_copy_g2s(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk, full);
+                mbar_arrive_expect_tx(fb, chunk * st.z);
+                for (int r = 0; r < st.z; ++r)
+                    bulk_copy_g2s(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk, fb);
             }
         } else {
             const uint32_t words = chunk >> 2;
-            for (int r = 0; r < st.nrows; ++r) {
+            for (int r = 0; r < st.z; ++r) {
                 const uint8_t* src = src0 + r * a.row_bytes;
                 uint32_t* dst = reinterpret_cast<uint32_t*>(dst0 + (size_t)r * a.rstride);
                 for (uint32_t w = lane; w < words; w += 32)
@@ -350,16 +474,18 @@ __global__ void __launch_bounds__(MAXT, MINB) q2k_mv_kernel(const MvArgs a)
             }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(full);
+                mbar_arrive(fb);
         }
+        if (lane == 0)
+            atomicAdd(n_issued, 1);
     };
-    int issued = 0;
     if (warp == 0) {
         const int pre = min(a.nst, nstages);
-        for (; issued < pre; ++issued)
-            produce(issued);
+        for (int i = 0; i < pre; ++i)
+            produce(i);
     }
 
+    // ---- this thread's slice ----
     const int g = tid / a.s_pad;           // row group
     const int sl_idx = tid - g * a.s_pad;  // slice within the row
     const bool active = sl_idx < a.s_real;
@@ -368,129 +494,148 @@ __global__ void __launch_bounds__(MAXT, MINB) q2k_mv_kernel(const MvArgs a)
     const int n = w0 >> 3;
     const int wi0 = w0 & 7;
     const int wig = sl_idx >> 5;  // warp index within the group
+    const int wl = a.s_pad < 32 ? a.s_pad : 32;
 
     S sl;
     int cur_e = -1;
-    float racc[RPT][M];
+    bool aborted = false;  // after a wait gave up: keep walking the stages
+                           // (segment-change barriers stay matched) but skip work
 
     for (int i = 0; i < nstages; ++i) {
         const int slot = i % a.nst;
-        const Stage st = stage_at(a, lo, hi, i);
+        const int4 st4 = tab[i];
+        const Stage st{st4.x, st4.y, st4.z};
         if (st.e != cur_e && (cur_e < 0 || a.x_seg_stride != 0)) {
-            load_slice<M, ACT, SW>(sl, a.x + (int64_t)st.e * a.x_seg_stride, a.x_tok_stride, a.kb0 + b, n, wi0,
-                                   active);
+            // uniform across the CTA: every warp walks the same stages
+            __syncthreads();  // everyone is done with the previous chunk
+            stage_x<M, ACT>(a.x + (int64_t)st.e * a.x_seg_stride, a.x_tok_stride, a.kb0, a.nbc, a.x_align, xsm);
+            __syncthreads();
+            load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         }
         cur_e = st.e;
-        bool ok = !*abort_flag;
-        if (ok) {
-            if (lane == 0)
-                ok = mbar_wait_bounded(smem_u32(&bars[slot]), (i / a.nst) & 1, abort_flag);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok && lane == 0)
-                flag_error(abort_flag);
+        if (aborted || !warp_wait(smem_u32(&full_b[slot]), (i / a.nst) & 1, abort_flag, lane)) {
+            aborted = true;
+            continue;
         }
+        const uint8_t* base = ring + (size_t)slot * a.stage_bytes + (size_t)b * kBlockBytes;
+
+        for (int s = 0; s < a.sub; ++s) {
+            const int rr0 = s * unit_rows;
+            if (rr0 >= st.nrows)
+                break;  // uniform: every warp skips the same units
+            const int u = i * a.sub + s;
+            float v[VP];
 #pragma unroll
-        for (int k = 0; k < RPT; ++k)
-#pragma unroll
-            for (int t = 0; t < M; ++t)
-                racc[k][t] = 0.f;
-        if (ok) {
-            const uint8_t* base = ring + (size_t)slot * a.stage_bytes + (size_t)b * kBlockBytes;
+            for (int q = 0; q < VP; ++q)
+                v[q] = 0.f;
 #pragma unroll
             for (int k = 0; k < RPT; ++k) {
-                const int rr = g + k * a.groups;
-                if (k < a.rpt && rr < st.nrows && active)
-                    slice_dot<M, ACT, SW>(sl, base + (size_t)rr * a.rstride, n, wi0, racc[k]);
+                const int rr = min(rr0 + g + k * a.groups, st.nrows - 1);  // past the end: recompute the last row
+                float acc[M];
+#pragma unroll
+                for (int t = 0; t < M; ++t)
+                    acc[t] = 0.f;
+                slice_dot<M, ACT, SW>(sl, base + (size_t)rr * a.rstride, n, wi0, acc);
+#pragma unroll
+                for (int t = 0; t < M; ++t)
+                    v[k * M + t] = acc[t];
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bars[a.nst + slot]));
-        }
-        // refill this slot with stage i + nst once every warp has released it
-        if (warp == 0 && issued < nstages) {
-            bool ok2 = !*abort_flag;
-            if (ok2) {
-                if (lane == 0)
-                    ok2 = mbar_wait_bounded(smem_u32(&bars[a.nst + slot]), (i / a.nst) & 1, abort_flag);
-                ok2 = __shfl_sync(0xffffffffu, ok2, 0);
-                if (!ok2 && lane == 0)
-                    flag_error(abort_flag);
-            }
-            if (ok2) {
-                produce(issued);
-                ++issued;
-            }
-        }
-        // reduce every (row slot, token) over the row group's lanes
-        const int width = a.s_pad < 32 ? a.s_pad : 32;
+            // reduce over the row group's lanes and deposit the warp's sums;
+            // they are added across warps once, after the stage loop
+            float* rb = red + (size_t)u * red_one;
+            if (wl == 32) {
+                const float r = transpose_reduce<VP>(v, lane);
+                constexpr int SH = 5 - log2_exact(VP);
+                if ((lane & ((1 << SH) - 1)) == 0)
+                    rb[(g * wpg + wig) * VP + (lane >> SH)] = r;
+            } else {
 #pragma unroll
-        for (int k = 0; k < RPT; ++k)
+                for (int q = 0; q < V; ++q)
+                    for (int o = wl >> 1; o > 0; o >>= 1)
+                        v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                if (sl_idx == 0) {
 #pragma unroll
-            for (int t = 0; t < M; ++t) {
-                float v = racc[k][t];
-                if (k < a.rpt)
-                    for (int o = width >> 1; o > 0; o >>= 1)
-                        v += __shfl_xor_sync(0xffffffffu, v, o);
-                racc[k][t] = v;
-            }
-        float* rbuf = red + (i & 1) * red_one;
-        if (wpg > 1) {
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < RPT; ++k)
-#pragma unroll
-                    for (int t = 0; t < M; ++t)
-                        rbuf[((g * RPT + k) * M + t) * wpg + wig] = racc[k][t];
-            }
-            __syncthreads();
-        }
-        // writer: thread (k*M + t) of the group (several warps), or the
-        // group's slice-0 lane (group within one warp)
-        if (ok) {
-#pragma unroll
-            for (int k = 0; k < RPT; ++k)
-#pragma unroll
-                for (int t = 0; t < M; ++t) {
-                    const int rr = g + k * a.groups;
-                    if (k >= a.rpt || rr >= st.nrows)
-                        continue;
-                    float v;
-                    if (wpg > 1) {
-                        if (sl_idx != k * M + t)
-                            continue;
-                        v = 0.f;
-                        const float* rp = rbuf + ((g * RPT + k) * M + t) * wpg;
-                        for (int q = 0; q < wpg; ++q)
-                            v += rp[q];
-                    } else {
-                        if (sl_idx != 0)
-                            continue;
-                        v = racc[k][t];
-                    }
-                    const int64_t row = st.row0 + rr;
-                    if (a.table) {
-                        if (a.y_exp) {
-                            float* yp = a.y_exp + (int64_t)st.e * a.N[0] + row;
-                            *yp = a.accumulate ? *yp + v : v;
-                        }
-                        if (a.y_sum)
-                            ysum[row - lo] = fmaf(a.route_w[st.e], v, ysum[row - lo]);
-                    } else {
-                        float* yp = a.y[st.e] + (int64_t)t * a.ldy[st.e] + row;
-                        *yp = a.accumulate ? *yp + v : v;
-                    }
+                    for (int q = 0; q < V; ++q)
+                        rb[g * VP + q] = v[q];
                 }
+            }
+        }
+        // release the slot; the last warp to release it refills it with
+        // stage i + nst, so no warp ever waits to produce
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&cnt[slot], 1) == nwarps - 1;
+            if (last)
+                cnt[slot] = 0;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && i + a.nst < nstages)
+            produce(i + a.nst);
+    }
+
+    // every issued copy must have landed before the CTA exits
+    __syncthreads();
+    if (*abort_flag) {
+        if (tid == 0) {
+            const int issued = *reinterpret_cast<volatile int*>(n_issued);
+            for (int i = max(0, issued - a.nst); i < issued; ++i)
+                mbar_wait_bounded(smem_u32(&full_b[i % a.nst]), (i / a.nst) & 1, nullptr);
+        }
+        __syncthreads();
+        return;
+    }
+
+    // ---- outputs: add the warps' partial sums of every (row, token) ----
+    // Unit u = i*sub + s holds rows s*unit_rows + g + k*groups of stage i,
+    // value index k*M + t, one partial per warp of the row group.
+    for (int i = 0; i < nstages; ++i) {
+        const int4 st4 = tab[i];
+        const Stage st{st4.x, st4.y, st4.z};
+        const int per_stage = a.sub * a.groups * V;
+        for (int p = tid; p < per_stage; p += blockDim.x) {
+            const int s2 = p / (a.groups * V);
+            const int rem = p - s2 * (a.groups * V);
+            const int g2 = rem / V, idx = rem - g2 * V;
+            const int k = idx / M, t = idx - k * M;
+            const int rr = s2 * unit_rows + g2 + k * a.groups;
+            if (rr >= st.nrows)
+                continue;
+            const float* rb = red + (size_t)(i * a.sub + s2) * red_one + g2 * wpg * VP + idx;
+            float v = 0.f;
+            for (int q = 0; q < wpg; ++q)
+                v += rb[q * VP];
+            const int row = st.row0 + rr;
+            if (a.table) {
+                if (a.y_exp) {
+                    float* yp = a.y_exp + (int64_t)st.e * a.N[0] + row;
+                    *yp = a.accumulate ? *yp + v : v;
+                }
+            } else {
+                float* yp = a.y[st.e] + (int64_t)t * a.ldy[st.e] + row;
+                *yp = a.accumulate ? *yp + v : v;
+            }
         }
     }
-    // every issued copy must have landed before the CTA exits
-    if (*abort_flag && warp == 0 && lane == 0) {
-        for (int i = max(0, issued - a.nst); i < issued; ++i)
-            mbar_wait_bounded(smem_u32(&bars[i % a.nst]), (i / a.nst) & 1, nullptr);
-    }
-    __syncthreads();
+    // fused route-weighted sum over the segments, in segment order
     if (a.table && a.y_sum) {
-        for (int r = tid; r < (int)(hi - lo); r += a.tc)
-            a.y_sum[lo + r] = ysum[r];
+        const int per = (hi - lo + a.rps - 1) / a.rps;  // stages per segment
+        for (int r = tid; r < hi - lo; r += blockDim.x) {
+            const int c = r / a.rps, rin = r - c * a.rps;  // stage within a segment, row within it
+            const int s2 = rin / unit_rows, rem = rin - s2 * unit_rows;
+            const int k = rem / a.groups, g2 = rem - k * a.groups;
+            const int idx = k * M;  // token 0 (experts run m = 1)
+            float acc = a.accumulate ? a.y_sum[lo + r] : 0.f;
+            for (int e = 0; e < a.n_seg; ++e) {
+                const float* rb = red + (size_t)((e * per + c) * a.sub + s2) * red_one + g2 * wpg * VP + idx;
+                float v = 0.f;
+                for (int q = 0; q < wpg; ++q)
+                    v += rb[q * VP];
+                acc = fmaf(a.route_w[e], v, acc);
+            }
+            a.y_sum[lo + r] = acc;
+        }
     }
 }
 
@@ -498,10 +643,10 @@ __global__ void __launch_bounds__(MAXT, MINB) q2k_mv_kernel(const MvArgs a)
 
 namespace {
 
-template <int M, int ACT, int SW, int MAXT, int MINB>
+template <int M, int ACT, int SW>
 cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
 {
-    auto k = q2k_mv_kernel<M, ACT, SW, MAXT, MINB>;
+    auto k = q2k_mv_kernel<M, ACT, SW>;
     static int configured_for = -1;  // device id the attribute was set for
     static size_t configured_smem = 0;
     int dev = 0;
@@ -526,22 +671,16 @@ int sw_for(int act, int m)
     return m <= 2 ? 4 : (m <= 4 ? 2 : 1);
 }
 
-int mchunk_max(int act) { return act == ACT_Q8 ? 8 : 8; }
-
-int nbc_max(int sw) { return sw == 4 ? 64 : (sw == 2 ? 64 : 32); }
-
 template <int ACT, int SW>
 cudaError_t dispatch_m(int m, const MvArgs& a, int grid, size_t smem, cudaStream_t s)
 {
-    constexpr int MAXT = SW == 4 ? 256 : 512;
-    constexpr int MINB = SW == 4 ? 2 : 1;
     switch (m) {
-#define Q2K_CASE(MM)                                                        \
-    case MM:                                                                \
-        if constexpr ((SW == 4 && (ACT == ACT_Q8 ? MM <= 4 : MM <= 2)) ||   \
+#define Q2K_CASE(MM)                                                                   \
+    case MM:                                                                           \
+        if constexpr ((SW == 4 && (ACT == ACT_Q8 ? MM <= 4 : MM <= 2)) ||              \
                       (SW == 2 && (ACT == ACT_Q8 ? MM >= 5 : (MM >= 3 && MM <= 4))) || \
-                      (SW == 1 && ACT == ACT_BF16 && MM >= 5))              \
-            return launch_one<MM, ACT, SW, MAXT, MINB>(a, grid, smem, s);   \
+                      (SW == 1 && ACT == ACT_BF16 && MM >= 5))                         \
+            return launch_one<MM, ACT, SW>(a, grid, smem, s);                          \
         break;
         Q2K_CASE(1) Q2K_CASE(2) Q2K_CASE(3) Q2K_CASE(4) Q2K_CASE(5) Q2K_CASE(6) Q2K_CASE(7) Q2K_CASE(8)
 #undef Q2K_CASE
@@ -563,6 +702,8 @@ cudaError_t dispatch(int act, int sw, int m, const MvArgs& a, int grid, size_t s
     return dispatch_m<ACT_BF16, 1>(m, a, grid, smem, s);
 }
 
+size_t align16(size_t v) { return (v + 15) / 16 * 16; }
+
 }  // namespace
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
@@ -572,89 +713,108 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
     if (err != cudaSuccess)
         return err;
     const int64_t nb = p.K / kBlockWeights;
-    const int64_t act_bytes_per_k = 0;  // (documentation only)
-    (void)act_bytes_per_k;
     const bool table = p.W_table != nullptr;
+    if (p.N[0] > (1 << 30) || p.N[1] > (1 << 30) || (int64_t)p.N[0] + p.N[1] > (1 << 30))
+        return cudaErrorInvalidValue;
 
-    // token chunks (all tokens in one chunk: the kernel family covers m <= 8)
-    for (int t0 = 0; t0 < p.m; t0 += mchunk_max(p.act)) {
-        const int mc = std::min(p.m - t0, mchunk_max(p.act));
-        const int sw = sw_for(p.act, mc);
-        const int spb = 16 / sw;
-        const int64_t nbcm = nbc_max(sw);
-        for (int64_t kb0 = 0; kb0 < nb; kb0 += nbcm) {
-            const int nbc = (int)std::min(nbcm, nb - kb0);
-            MvArgs a{};
-            a.n_seg = p.n_seg;
-            a.table = table ? 1 : 0;
-            a.W_table = p.W_table;
-            a.W[0] = static_cast<const uint8_t*>(p.W[0]);
-            a.W[1] = static_cast<const uint8_t*>(p.W[1]);
-            a.N[0] = p.N[0];
-            a.N[1] = p.N[1];
-            a.row_bytes = nb * kBlockBytes;
-            a.kb0 = (int)kb0;
-            a.nbc = nbc;
-            a.x = static_cast<const uint8_t*>(p.x) + (int64_t)t0 * p.x_tok_stride;
-            a.x_tok_stride = p.x_tok_stride;
-            a.x_seg_stride = p.x_seg_stride;
-            for (int e = 0; e < 2; ++e) {
-                a.y[e] = p.y[e] ? p.y[e] + (int64_t)t0 * p.ldy[e] : nullptr;
-                a.ldy[e] = p.ldy[e];
-            }
-            a.y_exp = p.y_exp;
-            a.route_w = p.route_w;
-            a.y_sum = p.y_sum;
-            a.accumulate = kb0 > 0 ? 1 : 0;
+    const int mc = p.m;  // the kernel family covers m <= 8 in one pass
+    const int sw = sw_for(p.act, mc);
+    const int spb = 16 / sw;
+    const int rpt = rpt_for(mc);
+    const int vp = pow2_ceil(rpt * mc);
+    const int xbpb = p.act == ACT_BF16 ? 512 : 8 * kQ8Bytes;  // staged bytes per token and block column
+    // blocks per K chunk: the slices of a row fit the CTA, and the staged
+    // activations take at most half of the shared memory
+    int64_t nbcm = kThreads * sw / 16;
+    while (nbcm > 1 && (int64_t)mc * nbcm * xbpb > 112 * 1024)
+        nbcm /= 2;
+    const size_t smem_cap = std::min<size_t>((size_t)di.smem_optin, 224 * 1024);
 
-            a.s_real = nbc * spb;
-            if (a.s_real <= 32) {
-                int sp = 1;
-                while (sp < a.s_real)
-                    sp <<= 1;
-                a.s_pad = sp;
-            } else {
-                a.s_pad = (a.s_real + 31) / 32 * 32;
-            }
-            const int tc_target = 256;
-            a.groups = std::max(1, tc_target / a.s_pad);
-            a.tc = a.groups * a.s_pad;
-            const int64_t chunk = (int64_t)nbc * kBlockBytes;
-            a.rstride = (uint32_t)((chunk + 15) / 16 * 16);
-            const int stage_target = 16384;
-            const int rmax = rpt_max(mc);
-            int rpt = (int)std::max<int64_t>(1, std::min<int64_t>(rmax, stage_target / ((int64_t)a.groups * a.rstride)));
-            a.rpt = rpt;
-            a.rps = a.groups * rpt;
-            a.stage_bytes = (uint32_t)a.rps * a.rstride;
-
-            const bool big = sw == 4;
-            const int ctas_per_sm = big ? 2 : 1;
-            const size_t smem_cap = std::min<size_t>((size_t)di.smem_optin, big ? 110 * 1024 : 220 * 1024);
-            a.rows_total = table ? p.N[0] : p.N[0] + (p.n_seg > 1 ? p.N[1] : 0);
-            int64_t grid = (int64_t)di.sm_count * ctas_per_sm;
-            // at least a couple of rows per CTA
-            grid = std::min<int64_t>(grid, std::max<int64_t>(1, a.rows_total / 2));
-            if (grid < 1)
-                grid = 1;
-            const int64_t rows_per_cta = (a.rows_total + grid - 1) / grid;
-            a.ysum_cap = (table && p.y_sum) ? (int)rows_per_cta : 0;
-
-            const int wpg = a.s_pad >= 32 ? a.s_pad / 32 : 1;
-            const size_t red_bytes = 2 * sizeof(float) * (size_t)a.groups * rmax * mc * wpg;
-            const size_t fixed = red_bytes + sizeof(float) * (size_t)a.ysum_cap;
-            int nst = (int)std::min<int64_t>(16, (int64_t)((smem_cap - fixed - 256) / (a.stage_bytes + 16)));
-            // no more stages than this CTA will ever fill
-            const int64_t max_stages = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
-            nst = (int)std::min<int64_t>(nst, std::max<int64_t>(2, max_stages));
-            if (nst < 2)
-                return cudaErrorInvalidConfiguration;
-            a.nst = nst;
-            const size_t smem = (size_t)nst * a.stage_bytes + (2 * nst + 2) * sizeof(uint64_t) + fixed;
-            err = dispatch(p.act, sw, mc, a, (int)grid, smem, s);
-            if (err != cudaSuccess)
-                return err;
+    for (int64_t kb0 = 0; kb0 < nb; kb0 += nbcm) {
+        const int nbc = (int)std::min(nbcm, nb - kb0);
+        MvArgs a{};
+        a.n_seg = p.n_seg;
+        a.table = table ? 1 : 0;
+        a.W_table = p.W_table;
+        a.W[0] = static_cast<const uint8_t*>(p.W[0]);
+        a.W[1] = static_cast<const uint8_t*>(p.W[1]);
+        a.N[0] = (int)p.N[0];
+        a.N[1] = (int)p.N[1];
+        a.row_bytes = nb * kBlockBytes;
+        a.kb0 = (int)kb0;
+        a.nbc = nbc;
+        a.x = static_cast<const uint8_t*>(p.x);
+        a.x_tok_stride = p.x_tok_stride;
+        a.x_seg_stride = p.x_seg_stride;
+        {
+            const uintptr_t bits = (reinterpret_cast<uintptr_t>(p.x) + (uintptr_t)(kb0 * xbpb)) |
+                                   (uintptr_t)(mc > 1 ? p.x_tok_stride : 0) | (uintptr_t)p.x_seg_stride;
+            a.x_align = (bits & 15u) == 0 ? 16 : ((bits & 3u) == 0 ? 4 : 2);
         }
+        for (int e = 0; e < 2; ++e) {
+            a.y[e] = p.y[e];
+            a.ldy[e] = p.ldy[e];
+        }
+        a.y_exp = p.y_exp;
+        a.route_w = p.route_w;
+        a.y_sum = p.y_sum;
+        a.accumulate = kb0 > 0 ? 1 : 0;
+
+        a.s_real = nbc * spb;
+        if (a.s_real <= 32) {
+            int sp = 1;
+            while (sp < a.s_real)
+                sp <<= 1;
+            a.s_pad = sp;
+        } else {
+            a.s_pad = (a.s_real + 31) / 32 * 32;
+        }
+        a.groups = std::max(1, kThreads / a.s_pad);
+        a.tc = a.groups * a.s_pad;  // <= kThreads, a multiple of 32
+        const int64_t chunk = (int64_t)nbc * kBlockBytes;
+        a.rstride = (uint32_t)((chunk + 15) / 16 * 16);
+        const int unit_rows = a.groups * rpt;
+        // stages of about 40 KB: several reduction units each
+        a.sub = (int)std::max<int64_t>(1, std::min<int64_t>(16, 40 * 1024 / ((int64_t)unit_rows * a.rstride)));
+
+        a.rows_total = table ? (int)p.N[0] : (int)(p.N[0] + (p.n_seg > 1 ? p.N[1] : 0));
+        const int wpg = a.s_pad >= 32 ? a.s_pad / 32 : 1;
+        int64_t grid = std::min<int64_t>(di.sm_count, std::max<int64_t>(1, a.rows_total / 2));
+        int64_t rows_per_cta = (a.rows_total + grid - 1) / grid;
+        // more CTAs (in waves) when one CTA's partial sums would not fit
+        const int64_t per_row = (int64_t)wpg * vp * (table ? p.n_seg : 1) * (int64_t)sizeof(float) / rpt + 1;
+        while (rows_per_cta * per_row > 48 * 1024 && rows_per_cta > (int64_t)unit_rows * a.sub) {
+            grid += di.sm_count;
+            rows_per_cta = (a.rows_total + grid - 1) / grid;
+        }
+        // a stage never holds more rows than the CTA owns
+        while (a.sub > 1 && (int64_t)unit_rows * a.sub / 2 >= rows_per_cta)
+            a.sub = (a.sub + 1) / 2;
+        a.rps = unit_rows * a.sub;
+        a.stage_bytes = (uint32_t)(a.rps * (int64_t)a.rstride);
+
+        const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
+        a.max_stages = (int)stages_per_cta;
+        const size_t x_bytes = align16((size_t)mc * nbc * xbpb);
+        const size_t red_bytes = sizeof(float) * (size_t)stages_per_cta * a.sub * a.groups * wpg * vp;
+        size_t smem = 0;
+        int nst = 8;
+        for (; nst >= 2; --nst) {
+            a.nst = (int)std::min<int64_t>(nst, std::max<int64_t>(2, stages_per_cta));
+            a.off_x = (uint32_t)((size_t)a.nst * a.stage_bytes);
+            a.off_bar = (uint32_t)(a.off_x + x_bytes);
+            a.off_tab = (uint32_t)align16(a.off_bar + (size_t)(a.nst + 1) * sizeof(uint64_t));
+            a.off_cnt = (uint32_t)align16(a.off_tab + (size_t)a.max_stages * sizeof(int4));
+            a.off_red = (uint32_t)align16(a.off_cnt + (size_t)(a.nst + 1) * sizeof(int));
+            smem = align16(a.off_red + red_bytes);
+            if (smem <= smem_cap)
+                break;
+        }
+        if (nst < 2)
+            return cudaErrorInvalidConfiguration;
+        err = dispatch(p.act, sw, mc, a, (int)grid, smem, s);
+        if (err != cudaSuccess)
+            return err;
     }
     return cudaSuccess;
 }

@@ -208,9 +208,13 @@ def test_mmvq_q8_1_small(lib, N, K, m):
     x = synth.bf16_normal(8, f"mmvq.x.{m}.{K}", (m, K))
     xq = oracle.q8_1_quantize(x)
     y = lib.q2k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
-    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
-    # diagnostic: against the exact projection of the values q8_1 encodes
+    # against the exact projection of the values the q8_1 rows encode
     assert rel_err_rows(y, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= 1e-4
+    # against the bf16 activations: the q8_1 gate, meaningful once the
+    # output row is long enough for its L2 norm to average the per-element
+    # quantisation noise (a single output is one noisy dot product)
+    if N >= 32:
+        assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
 
 
 @pytest.mark.parametrize("m", [1, 2, 4, 8])
