@@ -58,6 +58,7 @@ struct MvArgs {
     int64_t x_tok_stride;
     int64_t x_seg_stride;
     int x_align;  // 16, 4 or 2: widest copy the activation addresses allow
+    int x_bulk;   // 1: the first segment's activations arrive by bulk copy
     float* y[2];
     int64_t ldy[2];
     float* y_exp;
@@ -86,41 +87,6 @@ struct Stage {
     int nrows;
 };
 
-// Walks this CTA's stages: rows [lo, hi) of the row space, split at segment
-// ends (concat) or repeated for every segment (table).
-struct StageIter {
-    int e, r, end, lo, hi;
-    __device__ __forceinline__ void init(const MvArgs& a, int lo_, int hi_)
-    {
-        lo = lo_;
-        hi = hi_;
-        if (a.table || lo < a.N[0]) {
-            e = 0;
-            r = lo;
-            end = a.table ? hi : min(hi, a.N[0]);
-        } else {
-            e = 1;
-            r = lo - a.N[0];
-            end = hi - a.N[0];
-        }
-    }
-    __device__ __forceinline__ Stage get(const MvArgs& a) const { return Stage{e, r, min(a.rps, end - r)}; }
-    __device__ __forceinline__ void next(const MvArgs& a)
-    {
-        r += a.rps;
-        if (r < end)
-            return;
-        if (a.table) {
-            ++e;
-            r = lo;
-        } else if (e == 0 && hi > a.N[0]) {
-            e = 1;
-            r = max(lo, a.N[0]) - a.N[0];
-            end = hi - a.N[0];
-        }
-    }
-};
-
 __device__ __forceinline__ int stage_count(const MvArgs& a, int lo, int hi)
 {
     if (hi <= lo)
@@ -131,6 +97,27 @@ __device__ __forceinline__ int stage_count(const MvArgs& a, int lo, int hi)
     const int l0 = max(0, min(hi, n0) - lo);
     const int l1 = max(0, hi - max(lo, n0));
     return (l0 + a.rps - 1) / a.rps + (l1 + a.rps - 1) / a.rps;
+}
+
+// Stage i of the CTA owning rows [lo, hi): the rows split at the segment
+// end (concat: both matrices' rows one after the other) or repeated for
+// every segment (table), in chunks of rps rows.
+__device__ __forceinline__ Stage stage_at(const MvArgs& a, int lo, int hi, int i)
+{
+    if (a.table) {
+        const int per = (hi - lo + a.rps - 1) / a.rps;
+        const int e = i / per, c = i - e * per;
+        const int r = lo + c * a.rps;
+        return Stage{e, r, min(a.rps, hi - r)};
+    }
+    const int e0 = min(hi, a.N[0]);
+    const int c0 = e0 > lo ? (e0 - lo + a.rps - 1) / a.rps : 0;
+    if (i < c0) {
+        const int r = lo + i * a.rps;
+        return Stage{0, r, min(a.rps, e0 - r)};
+    }
+    const int r = max(lo, a.N[0]) - a.N[0] + (i - c0) * a.rps;
+    return Stage{1, r, min(a.rps, hi - a.N[0] - r)};
 }
 
 __device__ __forceinline__ const uint8_t* seg_weights(const MvArgs& a, int e)
@@ -421,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     uint8_t* ring = smem;
     uint8_t* xsm = smem + a.off_x;
     uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + a.off_bar);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(full_b + a.nst);
+    uint64_t* xbar = full_b + a.nst;  // the first activation chunk landed
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full_b + a.nst + 1);
     int4* tab = reinterpret_cast<int4*>(smem + a.off_tab);  // {e, row0, nrows, -} per stage
     int* cnt = reinterpret_cast<int*>(smem + a.off_cnt);    // warps done with each slot
     int* n_issued = cnt + a.nst;
@@ -434,17 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     if (tid == 0) {
         for (int s = 0; s < a.nst; ++s)
             mbar_init(smem_u32(&full_b[s]), 1);
+        mbar_init(smem_u32(xbar), 1);
         *abort_flag = 0;
-        StageIter it;
-        it.init(a, lo, hi);
-        for (int i = 0; i < nstages; ++i) {
-            const Stage st = it.get(a);
-            tab[i] = make_int4(st.e, st.row0, st.nrows, 0);
-            it.next(a);
-        }
         for (int s = 0; s <= a.nst; ++s)
             cnt[s] = 0;
         fence_mbar_init();
+    }
+    for (int i = tid; i < nstages; i += blockDim.x) {
+        const Stage st = stage_at(a, lo, hi, i);
+        tab[i] = make_int4(st.e, st.row0, st.nrows, 0);
     }
     __syncthreads();
 
@@ -479,10 +465,30 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (lane == 0)
             atomicAdd(n_issued, 1);
     };
+    // Activations first: the first segment's K chunk by bulk copy (ahead of
+    // the weight prefetch, so it does not queue behind it), weight stage 0,
+    // then the rest of the prefetch once the activations have landed.
+    const bool x_first_bulk = a.x_bulk && nstages > 0;
+    const int x_rowb = a.nbc * x_bytes_per_block<ACT>();
     if (warp == 0) {
         const int pre = min(a.nst, nstages);
-        for (int i = 0; i < pre; ++i)
-            produce(i);
+        if (x_first_bulk) {
+            if (lane == 0) {
+                const uint8_t* xs0 = a.x + (int64_t)tab[0].x * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
+                mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
+                for (int t = 0; t < M; ++t)
+                    bulk_copy_g2s(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
+                                  smem_u32(xbar));
+            }
+            if (pre > 0)
+                produce(0);
+            warp_wait(smem_u32(xbar), 0, abort_flag, lane);
+            for (int i = 1; i < pre; ++i)
+                produce(i);
+        } else {
+            for (int i = 0; i < pre; ++i)
+                produce(i);
+        }
     }
 
     // ---- this thread's slice ----
@@ -500,6 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     int cur_e = -1;
     bool aborted = false;  // after a wait gave up: keep walking the stages
                            // (segment-change barriers stay matched) but skip work
+    if (x_first_bulk) {
+        aborted = !warp_wait(smem_u32(xbar), 0, abort_flag, lane);
+        load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
+        cur_e = tab[0].x;
+    }
 
     for (int i = 0; i < nstages; ++i) {
         const int slot = i % a.nst;
@@ -582,6 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             const int issued = *reinterpret_cast<volatile int*>(n_issued);
             for (int i = max(0, issued - a.nst); i < issued; ++i)
                 mbar_wait_bounded(smem_u32(&full_b[i % a.nst]), (i / a.nst) & 1, nullptr);
+            if (x_first_bulk)
+                mbar_wait_bounded(smem_u32(xbar), 0, nullptr);
         }
         __syncthreads();
         return;
@@ -590,11 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     // ---- outputs: add the warps' partial sums of every (row, token) ----
     // Unit u = i*sub + s holds rows s*unit_rows + g + k*groups of stage i,
     // value index k*M + t, one partial per warp of the row group.
-    for (int i = 0; i < nstages; ++i) {
-        const int4 st4 = tab[i];
-        const Stage st{st4.x, st4.y, st4.z};
-        const int per_stage = a.sub * a.groups * V;
-        for (int p = tid; p < per_stage; p += blockDim.x) {
+    const int per_stage = a.sub * a.groups * V;
+    for (int q = tid; q < nstages * per_stage; q += blockDim.x) {
+        const int i = q / per_stage, p = q - i * per_stage;
+        {
+            const int4 st4 = tab[i];
+            const Stage st{st4.x, st4.y, st4.z};
             const int s2 = p / (a.groups * V);
             const int rem = p - s2 * (a.groups * V);
             const int g2 = rem / V, idx = rem - g2 * V;
@@ -750,6 +764,7 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
             const uintptr_t bits = (reinterpret_cast<uintptr_t>(p.x) + (uintptr_t)(kb0 * xbpb)) |
                                    (uintptr_t)(mc > 1 ? p.x_tok_stride : 0) | (uintptr_t)p.x_seg_stride;
             a.x_align = (bits & 15u) == 0 ? 16 : ((bits & 3u) == 0 ? 4 : 2);
+            a.x_bulk = a.x_align == 16 ? 1 : 0;
         }
         for (int e = 0; e < 2; ++e) {
             a.y[e] = p.y[e];
@@ -803,7 +818,7 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
             a.nst = (int)std::min<int64_t>(nst, std::max<int64_t>(2, stages_per_cta));
             a.off_x = (uint32_t)((size_t)a.nst * a.stage_bytes);
             a.off_bar = (uint32_t)(a.off_x + x_bytes);
-            a.off_tab = (uint32_t)align16(a.off_bar + (size_t)(a.nst + 1) * sizeof(uint64_t));
+            a.off_tab = (uint32_t)align16(a.off_bar + (size_t)(a.nst + 2) * sizeof(uint64_t));
             a.off_cnt = (uint32_t)align16(a.off_tab + (size_t)a.max_stages * sizeof(int4));
             a.off_red = (uint32_t)align16(a.off_cnt + (size_t)(a.nst + 1) * sizeof(int));
             smem = align16(a.off_red + red_bytes);
