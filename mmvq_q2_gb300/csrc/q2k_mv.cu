@@ -74,6 +74,7 @@ struct MvArgs {
     int rps;            // rows per stage = groups * RPT * sub
     int nst;            // stages in the ring
     int rows_total;     // concat: N0 + N1; table: N
+    int rows_q, rows_r; // rows_total = rows_q * grid + rows_r: CTA c owns rows_q (+1 if c < rows_r) rows
     int max_stages;     // stages of the largest CTA
     uint32_t rstride;   // shared-memory row stride (16-byte multiple)
     uint32_t stage_bytes;
@@ -415,8 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     int* n_issued = cnt + a.nst;
     float* red = reinterpret_cast<float*>(smem + a.off_red);
 
-    const int lo = (int)(((int64_t)a.rows_total * blockIdx.x) / gridDim.x);
-    const int hi = (int)(((int64_t)a.rows_total * (blockIdx.x + 1)) / gridDim.x);
+    const int cta = blockIdx.x;
+    const int lo = cta * a.rows_q + min(cta, a.rows_r);
+    const int hi = lo + a.rows_q + (cta < a.rows_r ? 1 : 0);
     const int nstages = stage_count(a, lo, hi);
 
     if (tid == 0) {
@@ -446,9 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         const bool tma = ((reinterpret_cast<uintptr_t>(src0) | (uintptr_t)a.row_bytes | chunk) & 15u) == 0;
         if (tma) {
             if (lane == 0) {
+                const uint64_t pol = l2_policy_evict_first();  // the weights are read once
                 mbar_arrive_expect_tx(fb, chunk * st.z);
-                for (int r = 0; r < st.z; ++r)
-                    bulk_copy_g2s(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk, fb);
+                if (chunk == a.rstride && (int64_t)chunk == a.row_bytes) {
+                    // whole rows, contiguous in global and in the ring: one copy
+                    bulk_copy_g2s_hint(smem_u32(dst0), src0, chunk * st.z, fb, pol);
+                } else {
+                    for (int r = 0; r < st.z; ++r)
+                        bulk_copy_g2s_hint(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk,
+                                           fb, pol);
+                }
             }
         } else {
             const uint32_t words = chunk >> 2;
@@ -475,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (x_first_bulk) {
             if (lane == 0) {
                 const uint8_t* xs0 = a.x + (int64_t)tab[0].x * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
+                const uint64_t pol = l2_policy_evict_last();  // every CTA reads the activations
                 mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
                 for (int t = 0; t < M; ++t)
-                    bulk_copy_g2s(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
-                                  smem_u32(xbar));
+                    bulk_copy_g2s_hint(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
+                                       smem_u32(xbar), pol);
             }
             if (pre > 0)
                 produce(0);
@@ -808,6 +818,8 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         a.rps = unit_rows * a.sub;
         a.stage_bytes = (uint32_t)(a.rps * (int64_t)a.rstride);
 
+        a.rows_q = (int)(a.rows_total / grid);
+        a.rows_r = (int)(a.rows_total % grid);
         const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
         a.max_stages = (int)stages_per_cta;
         const size_t x_bytes = align16((size_t)mc * nbc * xbpb);
