@@ -169,6 +169,27 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
                const uint16_t* x_bf16, const float* route_w, float* y, void* workspace,
                size_t workspace_bytes, q2k_stream_t stream);
 
+/* Size of the fixed device scratch behind q2k_moe_m1_static_scratch. */
+#define Q2K_MOE_M1_STATIC_SCRATCH_BYTES (1u << 20)
+
+/* q2k_moe_m1 without a caller workspace.  The pages have no counterpart:
+ * this is a library convenience for callers that cannot allocate device
+ * memory (no device allocator of their own, or memory planned once that
+ * must not grow between decode steps).
+ *   ptrs, E, dim, inter, x_bf16, route_w, y   as for q2k_moe_m1
+ * The workspace is a fixed Q2K_MOE_M1_STATIC_SCRATCH_BYTES (1 MiB) buffer
+ * in the library's device image; nothing is allocated or freed.  Problems
+ * with q2k_moe_m1_workspace_bytes(E, dim, inter) above that size return
+ * Q2K_ERR_WORKSPACE before anything is enqueued (E = 8, dim = 4096,
+ * inter = 2048 needs 154,112 bytes).  The first call on each device looks
+ * the scratch's address up (cudaGetSymbolAddress, which may load the
+ * module); make that first call before any stream capture.  Calls that
+ * overlap on one device share the scratch and race: issue them on one
+ * stream.  Results equal q2k_moe_m1's bit for bit. */
+int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
+                              const uint16_t* x_bf16, const float* route_w, float* y,
+                              q2k_stream_t stream);
+
 /* Dense bf16 GEMM on the tensor cores, any m >= 1 (engram_v41/apply.rs,
  * `ops::dense_gemm` for several tokens; moe_v41/init.rs `dense_gemm_bf16`).
  *   x bf16 [m, K], row stride ldx;  W bf16 [N, K] row-major;

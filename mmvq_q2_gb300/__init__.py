@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libq2k.so")
 EXPORTS = (
     "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16",
     "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_experts", "swiglu_q8_1_rows",
-    "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "dense_gemm_bf16", "q2k_status_string",
+    "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
     "q2k_last_cuda_error", "q2k_device_error",
 )
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "swiglu_q8_1_rows": (I32, [P, I64, I64, P, P, P]),
             "q2k_moe_m1_workspace_bytes": (SZ, [I64, I64, I64]),
             "q2k_moe_m1": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
+            "q2k_moe_m1_static_scratch": (I32, [P, I64, I64, I64, P, P, P, P]),
             "dense_gemm_bf16": (I32, [P, I64, I64, I64, P, I64, P, I64, P]),
             "q2k_status_string": (ctypes.c_char_p, [I32]),
             "q2k_last_cuda_error": (I32, []),
@@ -221,6 +222,17 @@ def q2k_moe_m1(ptrs, E, dim, inter, x, route_w, y=None, workspace=None, stream=N
     _call("q2k_moe_m1", _ptr(ptrs), E, dim, inter, _ptr(x), _ptr(route_w), _ptr(y), _ptr(workspace),
           workspace.numel(), _stream(stream))
     return y, workspace
+
+
+def q2k_moe_m1_static_scratch(ptrs, E, dim, inter, x, route_w, y=None, stream=None):
+    """As ``q2k_moe_m1`` on the library's fixed device scratch (no
+    workspace); calls on one device must not overlap."""
+    _need_cuda(ptrs, x, route_w, y)
+    if y is None:
+        y = torch.empty(dim, dtype=torch.float32, device=x.device)
+    _call("q2k_moe_m1_static_scratch", _ptr(ptrs), E, dim, inter, _ptr(x), _ptr(route_w), _ptr(y),
+          _stream(stream))
+    return y
 
 
 def dense_gemm_bf16(x, W, out=None, stream=None):

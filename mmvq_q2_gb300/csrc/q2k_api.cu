@@ -374,3 +374,69 @@ int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const 
 }
 
 }  // extern "C"
+
+// ---- routed experts without any allocation -------------------------------------
+//
+// Some callers cannot hand the library a workspace: a host program that links
+// only this library and has no device allocator of its own, or a decode loop
+// whose memory is planned once up front and must not allocate (or make its
+// allocator grow) between steps.  For them this entry point runs the same
+// four launches as q2k_moe_m1 on a fixed scratch buffer that lives in the
+// library's own device image.  The scratch is a file-scope __device__ array,
+// so it is reserved when the module loads: nothing is allocated or freed here.
+//
+// Every byte of the scratch is written before it is read within one call
+// (the q8_1 x, the fp32 gate/up outputs and the q8_1 h are produced in full
+// by their launches), so nothing has to be cleared.  Calls that overlap on
+// one device (two streams, or two threads) share this buffer and race; keep
+// them on one stream.
+
+namespace {
+__device__ __align__(256) unsigned char g_moe_scratch[Q2K_MOE_M1_STATIC_SCRATCH_BYTES];
+
+void* g_moe_scratch_ptr[kMaxDevices];
+std::mutex g_moe_scratch_mu;
+
+// The scratch's device address on the current device, looked up once per
+// device (the first call on a device does this; it may load the module).
+cudaError_t moe_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_moe_scratch_mu);
+    if (!g_moe_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_moe_scratch)) != cudaSuccess)
+            return e;
+        g_moe_scratch_ptr[dev] = p;
+    }
+    *out = g_moe_scratch_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+extern "C" int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
+                                         const uint16_t* x_bf16, const float* route_w, float* y,
+                                         q2k_stream_t stream)
+{
+    if (!ptrs || !x_bf16 || !route_w || !y)
+        return Q2K_ERR_NULL_ARG;
+    const size_t need = q2k_moe_m1_workspace_bytes(E, dim, inter);
+    if (need == 0)
+        return Q2K_ERR_BAD_SHAPE;
+    if (need > (size_t)Q2K_MOE_M1_STATIC_SCRATCH_BYTES)
+        return Q2K_ERR_WORKSPACE;  // the problem does not fit the fixed scratch
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    void* ws = nullptr;
+    cudaError_t e = moe_scratch(&ws);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    return q2k_moe_m1(ptrs, E, dim, inter, x_bf16, route_w, y, ws, (size_t)Q2K_MOE_M1_STATIC_SCRATCH_BYTES, stream);
+}
+
