@@ -59,6 +59,8 @@ struct MvArgs {
     int64_t x_seg_stride;
     int x_align;  // 16, 4 or 2: widest copy the activation addresses allow
     int x_bulk;   // 1: the first segment's activations arrive by bulk copy
+    int x_in_ring;  // 1: they arrive in the last ring slot, which the
+                    // weights take over once every warp holds its slice
     float* y[2];
     int64_t ldy[2];
     float* y_exp;
@@ -73,6 +75,7 @@ struct MvArgs {
     int sub;            // reduction units per stage
     int rps;            // rows per stage = groups * RPT * sub
     int nst;            // stages in the ring
+    uint32_t nst_magic; // ceil(2^32 / nst): i / nst == umulhi(i, nst_magic) for i < 2^24
     int rows_total;     // concat: N0 + N1; table: N
     int rows_q, rows_r; // rows_total = rows_q * grid + rows_r: CTA c owns rows_q (+1 if c < rows_r) rows
     int max_stages;     // stages of the largest CTA
@@ -195,6 +198,84 @@ __device__ __forceinline__ void stage_x(const uint8_t* xseg, int64_t tok_stride,
     }
 }
 
+// bf16 activations for m <= 2 are converted once per CTA, cooperatively:
+// 16-bit fixed point with one power-of-two exponent per group of 16 values
+// (the group of one Q2_K sub-block's codes in one bit plane).  The packed
+// words are stored word-major with an XOR swizzle, so the slice reads of a
+// warp (lanes 16 groups apart) fall in 32 different banks; the exponents
+// follow as one byte per group.
+template <int M, int ACT, int SW>
+__host__ __device__ constexpr bool coop_x() { return ACT == ACT_BF16 && SW == 4 && M <= 2; }
+
+__device__ __forceinline__ int x_group_swz(int G) { return G ^ (((G >> 5) & 3) << 1); }
+
+// Shared bytes the converted activations of m tokens take (words, then
+// exponent bytes).
+__host__ __device__ constexpr int coop_x_bytes(int m, int nbc) { return m * nbc * 512 + ((m * nbc * 16 + 15) / 16) * 16; }
+
+constexpr int kCoopGroupsPerThread = 4;  // m * nbc * 16 <= 4 * threads (checked on the host)
+
+template <int M>
+__device__ __forceinline__ void convert_x_bf16(uint8_t* xsm, int nbc)
+{
+    const int NG = nbc * 16;  // groups of 16 values per token
+    uint32_t pk[kCoopGroupsPerThread][8];
+    uint32_t ebv[kCoopGroupsPerThread];
+#pragma unroll
+    for (int k = 0; k < kCoopGroupsPerThread; ++k) {
+        const int q = threadIdx.x + k * blockDim.x;
+        ebv[k] = 0u;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            pk[k][w] = 0u;
+        if (q < M * NG) {
+            const uint8_t* src = xsm + (size_t)q * 32;  // token-major, 32 bytes per group
+            const uint4 u0 = *reinterpret_cast<const uint4*>(src);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(src + 16);
+            const uint32_t raw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float v[16];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[2 * i] = __uint_as_float(raw[i] << 16);
+                v[2 * i + 1] = __uint_as_float(raw[i] & 0xFFFF0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+            }
+            const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;  // biased exponent of amax
+            if (eb >= 27u) {
+                // x16 = x * 2^(141-eb): |x16| < 2^15, exact for the group's
+                // largest 2^8 range.  Adding 1.5*2^23 (ulp 1) rounds to the
+                // nearest integer, ties to even, and leaves it in the low
+                // mantissa bits as a 16-bit two's complement value.
+                const float scale = __uint_as_float((268u - eb) << 23);
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const uint32_t f0 = __float_as_uint(fmaf(v[2 * w], scale, 12582912.0f));
+                    const uint32_t f1 = __float_as_uint(fmaf(v[2 * w + 1], scale, 12582912.0f));
+                    pk[k][w] = __byte_perm(f0, f1, 0x5410u);
+                }
+                ebv[k] = eb;
+            }
+        }
+    }
+    __syncthreads();  // every group has been read before any is overwritten
+    uint32_t* words = reinterpret_cast<uint32_t*>(xsm);
+    uint8_t* ebs = xsm + (size_t)M * NG * 32;
+#pragma unroll
+    for (int k = 0; k < kCoopGroupsPerThread; ++k) {
+        const int q = threadIdx.x + k * blockDim.x;
+        if (q < M * NG) {
+            const int t = q / NG, G = q - t * NG;
+            uint32_t* wt = words + (size_t)t * NG * 8 + x_group_swz(G);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                wt[w * NG] = pk[k][w];
+            ebs[q] = (uint8_t)ebv[k];
+        }
+    }
+    __syncthreads();
+}
+
 // Build this thread's activation slice from the staged K chunk.  Slice
 // geometry: block b within the chunk, half n, first qs word wi0 (0..7).
 // Weight of (j, word w, byte i) is k = b*256 + 128n + 32j + 4w + i.
@@ -210,7 +291,24 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
         float xsum[S::NH][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if constexpr (ACT == ACT_BF16) {
+            if constexpr (coop_x<M, ACT, SW>()) {
+                // converted words of group (b, n, j, h); the thread takes all 16 values
+                const int NG = nbc * 16;
+                const int G = b * 16 + 8 * n + 2 * j + (wi0 >> 2);
+                const uint32_t* wt = reinterpret_cast<const uint32_t*>(xsm) + (size_t)t * NG * 8 + x_group_swz(G);
+                const uint32_t eb = active ? (uint32_t)xsm[(size_t)M * NG * 32 + (size_t)t * NG + G] : 0u;
+                int sum = 0;
+#pragma unroll
+                for (int wl = 0; wl < 4; ++wl) {
+                    const uint32_t p0 = active ? wt[(2 * wl) * NG] : 0u;
+                    const uint32_t p1 = active ? wt[(2 * wl + 1) * NG] : 0u;
+                    sum = dp2a_lo_su(p0, 0x0101u, dp2a_lo_su(p1, 0x0101u, sum));
+                    sl.xa[t][j][wl][0] = p0;
+                    sl.xa[t][j][wl][1] = p1;
+                }
+                sl.xp[t][j][0] = eb >= 27u ? __uint_as_float((eb - 14u - 2u * j) << 23) : 0.f;
+                xsum[0][j] = eb >= 27u ? (float)sum * __uint_as_float((eb - 14u) << 23) : 0.f;
+            } else if constexpr (ACT == ACT_BF16) {
 #pragma unroll
                 for (int hh = 0; hh < S::NH; ++hh) {
                     // S::WPH*4 consecutive bf16 values, 8*WPH bytes, aligned to 8*WPH
@@ -246,16 +344,20 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
                         // x16 = x * 2^(141-eb): |x16| < 2^15, exact for the group's
                         // largest 2^8 range; xp = 2^(eb-141) * 4^-j.
                         const float scale = __uint_as_float((268u - eb) << 23);
+                        // round x*scale to an integer by adding 1.5*2^23 (its
+                        // ulp is 1; ties to even, as rint): the integer is then
+                        // the low mantissa bits, two's complement in 16 bits
 #pragma unroll
                         for (int wl = 0; wl < S::WPH; ++wl) {
-                            int q[4];
+                            uint32_t f[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                q[i] = __float2int_rn(v[wl * 4 + i] * scale);
-                                sum += q[i];
-                            }
-                            sl.xa[t][j][hh * S::WPH + wl][0] = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[1] << 16);
-                            sl.xa[t][j][hh * S::WPH + wl][1] = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
+                            for (int i = 0; i < 4; ++i)
+                                f[i] = __float_as_uint(fmaf(v[wl * 4 + i], scale, 12582912.0f));
+                            const uint32_t p0 = __byte_perm(f[0], f[1], 0x5410u);
+                            const uint32_t p1 = __byte_perm(f[2], f[3], 0x5410u);
+                            sum = dp2a_lo_su(p0, 0x0101u, dp2a_lo_su(p1, 0x0101u, sum));
+                            sl.xa[t][j][hh * S::WPH + wl][0] = p0;
+                            sl.xa[t][j][hh * S::WPH + wl][1] = p1;
                         }
                         sl.xp[t][j][hh] = __uint_as_float((eb - 14u - 2u * j) << 23);
                         xsum[hh][j] = (float)sum * __uint_as_float((eb - 14u) << 23);
@@ -396,6 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     constexpr int V = RPT * M;        // partial sums per thread per unit
     constexpr int VP = pow2_ceil(V);  // padded to a power of two (<= 32)
 
+    // Read one field from every 32 bytes of the parameter block up front:
+    // their first (cold) reads then overlap instead of queuing one after
+    // another behind the dependent index arithmetic below.
+    asm volatile("" ::"r"(a.n_seg), "r"(a.N[0]), "l"(a.x_tok_stride), "l"(a.y[0]), "l"(a.y_exp), "r"(a.s_pad),
+                 "r"(a.rows_r), "r"(a.off_red));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = a.tc >> 5;
@@ -405,21 +512,32 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
 
     // shared layout (offsets from the host, 16-byte aligned): weight ring |
     // staged activations | full barriers, abort flag | stage table |
-    // release counters, copies issued | partial sums of every unit
+    // release counters, copies issued, next stage to issue | partial sums
+    // of every unit
     uint8_t* ring = smem;
-    uint8_t* xsm = smem + a.off_x;
+    uint8_t* xsm = a.x_in_ring ? ring + (size_t)(a.nst - 1) * a.stage_bytes : smem + a.off_x;
     uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + a.off_bar);
     uint64_t* xbar = full_b + a.nst;  // the first activation chunk landed
     volatile int* abort_flag = reinterpret_cast<volatile int*>(full_b + a.nst + 1);
     int4* tab = reinterpret_cast<int4*>(smem + a.off_tab);  // {e, row0, nrows, -} per stage
-    int* cnt = reinterpret_cast<int*>(smem + a.off_cnt);    // warps done with each slot
+    int* cnt = reinterpret_cast<int*>(smem + a.off_cnt);    // warps done with each slot's stage
     int* n_issued = cnt + a.nst;
+    int* next_issue = cnt + a.nst + 1;  // the next stage to copy in
     float* red = reinterpret_cast<float*>(smem + a.off_red);
 
     const int cta = blockIdx.x;
     const int lo = cta * a.rows_q + min(cta, a.rows_r);
     const int hi = lo + a.rows_q + (cta < a.rows_r ? 1 : 0);
     const int nstages = stage_count(a, lo, hi);
+    const int pre = min(a.x_in_ring ? a.nst - 1 : a.nst, nstages);  // stages copied in by the prologue
+    // ring slot and phase parity of stage i, without a division
+    auto ring_pos = [&](int i, int& slot, uint32_t& parity) {
+        const int q = (int)__umulhi((uint32_t)i, a.nst_magic);
+        slot = i - q * a.nst;
+        parity = (uint32_t)q & 1u;
+    };
+    const bool x_first_bulk = a.x_bulk && nstages > 0;
+    const int x_rowb = a.nbc * x_bytes_per_block<ACT>();
 
     if (tid == 0) {
         for (int s = 0; s < a.nst; ++s)
@@ -428,7 +546,18 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         *abort_flag = 0;
         for (int s = 0; s <= a.nst; ++s)
             cnt[s] = 0;
+        *next_issue = pre;
         fence_mbar_init();
+        if (x_first_bulk) {
+            // the activations first, ahead of the weight prefetch
+            const int e0 = stage_at(a, lo, hi, 0).e;
+            const uint8_t* xs0 = a.x + (int64_t)e0 * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
+            const uint64_t pol = l2_policy_evict_last();  // every CTA reads them
+            mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
+            for (int t = 0; t < M; ++t)
+                bulk_copy_g2s_hint(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
+                                   smem_u32(xbar), pol);
+        }
     }
     for (int i = tid; i < nstages; i += blockDim.x) {
         const Stage st = stage_at(a, lo, hi, i);
@@ -440,7 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     // by lane 0; the 4-byte fallback uses the whole warp. ----
     const uint32_t chunk = (uint32_t)a.nbc * kBlockBytes;
     auto produce = [&](int i) {
-        const int slot = i % a.nst;
+        int slot;
+        uint32_t parity;
+        ring_pos(i, slot, parity);
         const int4 st = tab[i];
         const uint8_t* src0 = seg_weights(a, st.x) + (int64_t)st.y * a.row_bytes + (int64_t)a.kb0 * kBlockBytes;
         uint8_t* dst0 = ring + (size_t)slot * a.stage_bytes;
@@ -474,32 +605,54 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (lane == 0)
             atomicAdd(n_issued, 1);
     };
-    // Activations first: the first segment's K chunk by bulk copy (ahead of
-    // the weight prefetch, so it does not queue behind it), weight stage 0,
-    // then the rest of the prefetch once the activations have landed.
-    const bool x_first_bulk = a.x_bulk && nstages > 0;
-    const int x_rowb = a.nbc * x_bytes_per_block<ACT>();
-    if (warp == 0) {
-        const int pre = min(a.nst, nstages);
-        if (x_first_bulk) {
-            if (lane == 0) {
-                const uint8_t* xs0 = a.x + (int64_t)tab[0].x * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
-                const uint64_t pol = l2_policy_evict_last();  // every CTA reads the activations
-                mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
-                for (int t = 0; t < M; ++t)
-                    bulk_copy_g2s_hint(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
-                                       smem_u32(xbar), pol);
+    // Refills are claimed by whichever warp gets there first, so the cost of
+    // issuing a copy does not settle on one warp: a stage can be copied in
+    // once every warp has released its slot's previous stage.
+    auto try_issue = [&]() {
+        int claim = -1;
+        if (lane == 0) {
+            const int j = *reinterpret_cast<volatile int*>(next_issue);
+            if (j < nstages) {
+                int sj;  // a.nst >= 2
+                uint32_t pj;
+                ring_pos(j, sj, pj);
+                if (*reinterpret_cast<volatile int*>(&cnt[sj]) == nwarps && atomicCAS(next_issue, j, j + 1) == j) {
+                    atomicExch(&cnt[sj], 0);
+                    __threadfence_block();
+                    claim = j;
+                }
             }
-            if (pre > 0)
-                produce(0);
-            warp_wait(smem_u32(xbar), 0, abort_flag, lane);
-            for (int i = 1; i < pre; ++i)
-                produce(i);
-        } else {
-            for (int i = 0; i < pre; ++i)
-                produce(i);
         }
-    }
+        claim = __shfl_sync(0xffffffffu, claim, 0);
+        if (claim >= 0)
+            produce(claim);
+    };
+    // Wait for a weight stage; a waiting warp claims refills meanwhile.
+    // Gives up (and raises the abort flag) after about two seconds.
+    auto wait_stage = [&](int slot, uint32_t parity) -> bool {
+        const uint32_t bar = smem_u32(&full_b[slot]);
+        uint64_t t0 = 0;
+        for (uint32_t it = 0;; ++it) {
+            if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+                return true;
+            try_issue();
+            if ((it & 15u) == 15u) {
+                if (*abort_flag)
+                    return false;
+                const uint64_t now = global_timer_ns();
+                if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > 2000000000ull) {
+                    if (lane == 0)
+                        flag_error(abort_flag);
+                    return false;
+                }
+            }
+        }
+    };
+    // the first stages, one copy per warp, behind the activations
+    if (warp < pre)
+        produce(warp);
 
     // ---- this thread's slice ----
     const int g = tid / a.s_pad;           // row group
@@ -518,12 +671,24 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
                            // (segment-change barriers stay matched) but skip work
     if (x_first_bulk) {
         aborted = !warp_wait(smem_u32(xbar), 0, abort_flag, lane);
+        if constexpr (coop_x<M, ACT, SW>())
+            convert_x_bf16<M>(xsm, a.nbc);  // every thread (the condition is uniform)
         load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         cur_e = tab[0].x;
+        if (a.x_in_ring) {
+            // the activations now sit in registers: release their slot
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                atomicAdd(&cnt[a.nst - 1], 1);
+            }
+        }
     }
 
     for (int i = 0; i < nstages; ++i) {
-        const int slot = i % a.nst;
+        int slot;
+        uint32_t parity;
+        ring_pos(i, slot, parity);
         const int4 st4 = tab[i];
         const Stage st{st4.x, st4.y, st4.z};
         if (st.e != cur_e && (cur_e < 0 || a.x_seg_stride != 0)) {
@@ -531,10 +696,14 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             __syncthreads();  // everyone is done with the previous chunk
             stage_x<M, ACT>(a.x + (int64_t)st.e * a.x_seg_stride, a.x_tok_stride, a.kb0, a.nbc, a.x_align, xsm);
             __syncthreads();
+            if constexpr (coop_x<M, ACT, SW>())
+                convert_x_bf16<M>(xsm, a.nbc);
             load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         }
         cur_e = st.e;
-        if (aborted || !warp_wait(smem_u32(&full_b[slot]), (i / a.nst) & 1, abort_flag, lane)) {
+        if (!aborted)
+            try_issue();
+        if (aborted || !wait_stage(slot, parity)) {
             aborted = true;
             continue;
         }
@@ -551,15 +720,17 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
                 v[q] = 0.f;
 #pragma unroll
             for (int k = 0; k < RPT; ++k) {
-                const int rr = min(rr0 + g + k * a.groups, st.nrows - 1);  // past the end: recompute the last row
-                float acc[M];
+                const int rr = rr0 + g + k * a.groups;
+                if (rr < st.nrows) {  // uniform within a row group
+                    float acc[M];
 #pragma unroll
-                for (int t = 0; t < M; ++t)
-                    acc[t] = 0.f;
-                slice_dot<M, ACT, SW>(sl, base + (size_t)rr * a.rstride, n, wi0, acc);
+                    for (int t = 0; t < M; ++t)
+                        acc[t] = 0.f;
+                    slice_dot<M, ACT, SW>(sl, base + (size_t)rr * a.rstride, n, wi0, acc);
 #pragma unroll
-                for (int t = 0; t < M; ++t)
-                    v[k * M + t] = acc[t];
+                    for (int t = 0; t < M; ++t)
+                        v[k * M + t] = acc[t];
+                }
             }
             // reduce over the row group's lanes and deposit the warp's sums;
             // they are added across warps once, after the stage loop
@@ -581,19 +752,12 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
                 }
             }
         }
-        // release the slot; the last warp to release it refills it with
-        // stage i + nst, so no warp ever waits to produce
+        // release the slot (its refill is claimed by the next warp to look)
         __syncwarp();
-        int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&cnt[slot], 1) == nwarps - 1;
-            if (last)
-                cnt[slot] = 0;
+            atomicAdd(&cnt[slot], 1);
         }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && i + a.nst < nstages)
-            produce(i + a.nst);
     }
 
     // every issued copy must have landed before the CTA exits
@@ -601,8 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     if (*abort_flag) {
         if (tid == 0) {
             const int issued = *reinterpret_cast<volatile int*>(n_issued);
-            for (int i = max(0, issued - a.nst); i < issued; ++i)
-                mbar_wait_bounded(smem_u32(&full_b[i % a.nst]), (i / a.nst) & 1, nullptr);
+            for (int i = max(0, issued - a.nst); i < issued; ++i) {
+                int slot;
+                uint32_t parity;
+                ring_pos(i, slot, parity);
+                mbar_wait_bounded(smem_u32(&full_b[slot]), parity, nullptr);
+            }
             if (x_first_bulk)
                 mbar_wait_bounded(smem_u32(xbar), 0, nullptr);
         }
@@ -822,23 +990,29 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         a.rows_r = (int)(a.rows_total % grid);
         const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
         a.max_stages = (int)stages_per_cta;
-        const size_t x_bytes = align16((size_t)mc * nbc * xbpb);
+        const bool coop = p.act == ACT_BF16 && sw == 4 && mc <= 2;
+        if (coop && (int64_t)mc * nbc * 16 > (int64_t)kCoopGroupsPerThread * a.tc)
+            return cudaErrorInvalidConfiguration;  // not reached: tc >= 4 * nbc and groups >= 2 for m = 2
+        const size_t x_bytes = coop ? align16((size_t)coop_x_bytes(mc, nbc)) : align16((size_t)mc * nbc * xbpb);
+        // a single activation chunk, read once: stage it in the last ring slot
+        a.x_in_ring = (a.x_bulk && (p.x_seg_stride == 0 || p.n_seg == 1) && x_bytes <= a.stage_bytes) ? 1 : 0;
         const size_t red_bytes = sizeof(float) * (size_t)stages_per_cta * a.sub * a.groups * wpg * vp;
         size_t smem = 0;
         int nst = 8;
         for (; nst >= 2; --nst) {
-            a.nst = (int)std::min<int64_t>(nst, std::max<int64_t>(2, stages_per_cta));
+            a.nst = (int)std::min<int64_t>(nst, std::max<int64_t>(2, stages_per_cta + a.x_in_ring));
             a.off_x = (uint32_t)((size_t)a.nst * a.stage_bytes);
-            a.off_bar = (uint32_t)(a.off_x + x_bytes);
+            a.off_bar = (uint32_t)(a.off_x + (a.x_in_ring ? 0 : x_bytes));
             a.off_tab = (uint32_t)align16(a.off_bar + (size_t)(a.nst + 2) * sizeof(uint64_t));
             a.off_cnt = (uint32_t)align16(a.off_tab + (size_t)a.max_stages * sizeof(int4));
-            a.off_red = (uint32_t)align16(a.off_cnt + (size_t)(a.nst + 1) * sizeof(int));
+            a.off_red = (uint32_t)align16(a.off_cnt + (size_t)(a.nst + 2) * sizeof(int));
             smem = align16(a.off_red + red_bytes);
             if (smem <= smem_cap)
                 break;
         }
         if (nst < 2)
             return cudaErrorInvalidConfiguration;
+        a.nst_magic = (uint32_t)((0x100000000ull + (uint64_t)a.nst - 1) / (uint64_t)a.nst);
         err = dispatch(p.act, sw, mc, a, (int)grid, smem, s);
         if (err != cudaSuccess)
             return err;
