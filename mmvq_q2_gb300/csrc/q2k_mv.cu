@@ -539,15 +539,46 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     const bool x_first_bulk = a.x_bulk && nstages > 0;
     const int x_rowb = a.nbc * x_bytes_per_block<ACT>();
 
-    if (tid == 0) {
-        for (int s = 0; s < a.nst; ++s)
+    const uint32_t chunk = (uint32_t)a.nbc * kBlockBytes;
+    // Bulk copy of stage st into a ring slot (lane 0 only; the source rows
+    // start on 16-byte boundaries).
+    auto copy_stage = [&](int slot, const int4 st, const uint8_t* src0) {
+        uint8_t* dst0 = ring + (size_t)slot * a.stage_bytes;
+        const uint32_t fb = smem_u32(&full_b[slot]);
+        const uint64_t pol = l2_policy_evict_first();  // the weights are read once
+        mbar_arrive_expect_tx(fb, chunk * st.z);
+        if (chunk == a.rstride && (int64_t)chunk == a.row_bytes) {
+            // whole rows, contiguous in global and in the ring: one copy
+            bulk_copy_g2s_hint(smem_u32(dst0), src0, chunk * st.z, fb, pol);
+        } else {
+            for (int r = 0; r < st.z; ++r)
+                bulk_copy_g2s_hint(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk, fb, pol);
+        }
+    };
+    auto stage_src = [&](const int4 st) {
+        return seg_weights(a, st.x) + (int64_t)st.y * a.row_bytes + (int64_t)a.kb0 * kBlockBytes;
+    };
+    auto src_aligned = [&](const uint8_t* src0) {
+        return ((reinterpret_cast<uintptr_t>(src0) | (uintptr_t)a.row_bytes | chunk) & 15u) == 0;
+    };
+
+    // Prologue, before the first barrier: lane 0 of warp w sets up slot w's
+    // barrier and copies in stage w at once (warp 0 first the activations),
+    // so the first bytes are requested as early as possible.
+    bool early = false;  // this warp's prologue stage went out here
+    if (lane == 0) {
+        if (tid == 0) {
+            mbar_init(smem_u32(xbar), 1);
+            *abort_flag = 0;
+            for (int s = 0; s <= a.nst; ++s)
+                cnt[s] = 0;
+            *next_issue = pre;
+        }
+        for (int s = warp; s < a.nst; s += nwarps)
             mbar_init(smem_u32(&full_b[s]), 1);
-        mbar_init(smem_u32(xbar), 1);
-        *abort_flag = 0;
-        for (int s = 0; s <= a.nst; ++s)
-            cnt[s] = 0;
-        *next_issue = pre;
         fence_mbar_init();
+    }
+    if (tid == 0) {
         if (x_first_bulk) {
             // the activations first, ahead of the weight prefetch
             const int e0 = stage_at(a, lo, hi, 0).e;
@@ -559,6 +590,18 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
                                    smem_u32(xbar), pol);
         }
     }
+    // The first stage goes out right behind the activations; the other
+    // prologue stages wait until the activations have landed, so that the
+    // copy engine serves the bytes needed first, first.
+    const bool issue_now = warp < pre && (warp == 0 || !x_first_bulk);
+    if (issue_now) {
+        const Stage st0 = stage_at(a, lo, hi, warp);
+        const int4 st = make_int4(st0.e, st0.row0, st0.nrows, 0);
+        const uint8_t* src0 = stage_src(st);
+        early = src_aligned(src0);  // uniform within the warp
+        if (early && lane == 0)
+            copy_stage(warp, st, src0);
+    }
     for (int i = tid; i < nstages; i += blockDim.x) {
         const Stage st = stage_at(a, lo, hi, i);
         tab[i] = make_int4(st.e, st.row0, st.nrows, 0);
@@ -567,29 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
 
     // ---- producer role: stage i into slot i % nst.  Bulk copies are issued
     // by lane 0; the 4-byte fallback uses the whole warp. ----
-    const uint32_t chunk = (uint32_t)a.nbc * kBlockBytes;
     auto produce = [&](int i) {
         int slot;
         uint32_t parity;
         ring_pos(i, slot, parity);
         const int4 st = tab[i];
-        const uint8_t* src0 = seg_weights(a, st.x) + (int64_t)st.y * a.row_bytes + (int64_t)a.kb0 * kBlockBytes;
+        const uint8_t* src0 = stage_src(st);
         uint8_t* dst0 = ring + (size_t)slot * a.stage_bytes;
         const uint32_t fb = smem_u32(&full_b[slot]);
-        const bool tma = ((reinterpret_cast<uintptr_t>(src0) | (uintptr_t)a.row_bytes | chunk) & 15u) == 0;
-        if (tma) {
-            if (lane == 0) {
-                const uint64_t pol = l2_policy_evict_first();  // the weights are read once
-                mbar_arrive_expect_tx(fb, chunk * st.z);
-                if (chunk == a.rstride && (int64_t)chunk == a.row_bytes) {
-                    // whole rows, contiguous in global and in the ring: one copy
-                    bulk_copy_g2s_hint(smem_u32(dst0), src0, chunk * st.z, fb, pol);
-                } else {
-                    for (int r = 0; r < st.z; ++r)
-                        bulk_copy_g2s_hint(smem_u32(dst0 + (size_t)r * a.rstride), src0 + r * a.row_bytes, chunk,
-                                           fb, pol);
-                }
-            }
+        if (src_aligned(src0)) {
+            if (lane == 0)
+                copy_stage(slot, st, src0);
         } else {
             const uint32_t words = chunk >> 2;
             for (int r = 0; r < st.z; ++r) {
@@ -627,15 +658,18 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (claim >= 0)
             produce(claim);
     };
-    // Wait for a weight stage; a waiting warp claims refills meanwhile.
-    // Gives up (and raises the abort flag) after about two seconds.
+    // Wait for a weight stage.  A waiting warp polls (a short sleep between
+    // polls) and claims refills meanwhile, so slots freed by slower warps
+    // are refilled by the warps that are ahead.  Gives up (and raises the
+    // abort flag) after about two seconds.
     auto wait_stage = [&](int slot, uint32_t parity) -> bool {
         const uint32_t bar = smem_u32(&full_b[slot]);
         uint64_t t0 = 0;
         for (uint32_t it = 0;; ++it) {
-            if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+            if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity)))
                 return true;
             try_issue();
+            __nanosleep(64);
             if ((it & 15u) == 15u) {
                 if (*abort_flag)
                     return false;
@@ -650,9 +684,16 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             }
         }
     };
-    // the first stages, one copy per warp, behind the activations
-    if (warp < pre)
-        produce(warp);
+    // prologue stages issued before the barrier are counted now; those whose
+    // rows are not 16-byte aligned go out now (whole-warp copies)
+    if (issue_now) {
+        if (early) {
+            if (lane == 0)
+                atomicAdd(n_issued, 1);
+        } else {
+            produce(warp);
+        }
+    }
 
     // ---- this thread's slice ----
     const int g = tid / a.s_pad;           // row group
@@ -671,6 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
                            // (segment-change barriers stay matched) but skip work
     if (x_first_bulk) {
         aborted = !warp_wait(smem_u32(xbar), 0, abort_flag, lane);
+        if (warp > 0 && warp < pre)
+            produce(warp);  // the rest of the prologue stages, now the activations are in
         if constexpr (coop_x<M, ACT, SW>())
             convert_x_bf16<M>(xsm, a.nbc);  // every thread (the condition is uniform)
         load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
@@ -685,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         }
     }
 
+    bool released_last = false;  // this warp freed a slot last time round
     for (int i = 0; i < nstages; ++i) {
         int slot;
         uint32_t parity;
@@ -701,7 +745,9 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         }
         cur_e = st.e;
-        if (!aborted)
+        // the warp that freed a slot last is the one behind: leave the
+        // refill to a warp that is ahead (or waiting)
+        if (!aborted && !released_last)
             try_issue();
         if (aborted || !wait_stage(slot, parity)) {
             aborted = true;
@@ -754,10 +800,12 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         }
         // release the slot (its refill is claimed by the next warp to look)
         __syncwarp();
+        int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            atomicAdd(&cnt[slot], 1);
+            last = atomicAdd(&cnt[slot], 1) == nwarps - 1;
         }
+        released_last = __shfl_sync(0xffffffffu, last, 0) != 0;
     }
 
     // every issued copy must have landed before the CTA exits
