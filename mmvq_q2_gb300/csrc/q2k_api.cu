@@ -119,13 +119,15 @@ int q2k_device_error(int32_t* host_out, int clear)
 {
     if (!host_out)
         return Q2K_ERR_NULL_ARG;
-    int32_t a = 0, b = 0;
+    int32_t a = 0, b = 0, c = 0;
     cudaError_t e = mv_error_word(&a, clear != 0);
     if (e == cudaSuccess)
         e = gemm_error_word(&b, clear != 0);
+    if (e == cudaSuccess)
+        e = mt_error_word(&c, clear != 0);
     if (e != cudaSuccess)
         return fail_cuda(e);
-    *host_out = a | b;
+    *host_out = a | b | c;
     return Q2K_OK;
 }
 

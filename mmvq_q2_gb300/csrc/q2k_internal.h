@@ -40,6 +40,9 @@ struct MvProblem {
 };
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
+// Several tokens (m = 2..8, explicit segments) on the tensor cores.
+bool mt_supported(const MvProblem& p);
+cudaError_t launch_mt(const MvProblem& p, cudaStream_t s);
 
 cudaError_t launch_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids,
                                 int64_t n_rows, uint16_t* out, int32_t* err_flag, cudaStream_t s);
@@ -53,5 +56,6 @@ cudaError_t launch_dense_gemm(const uint16_t* x, int64_t m, int64_t K, int64_t l
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
 cudaError_t gemm_error_word(int32_t* out, bool clear);
+cudaError_t mt_error_word(int32_t* out, bool clear);
 
 }  // namespace q2k

@@ -948,6 +948,8 @@ size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
 {
+    if (mt_supported(p))
+        return launch_mt(p, s);  // several tokens: the tensor-core kernel
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess)

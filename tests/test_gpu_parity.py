@@ -258,6 +258,24 @@ def test_pair_ragged_sizes(lib):
     assert torch.equal(yb, lib.q2k_mmvq_q8_1(dev(Wb), xq, K))
 
 
+@pytest.mark.parametrize("m,K", [(6, 8448), (8, 16384)])
+def test_pair_several_tokens_long_k(lib, m, K):
+    # several tokens and several K chunks (the tensor-core path): each output
+    # still equals the single call bit for bit, and matches the oracle
+    Wa = synth.q2k_matrix(5, f"prl.a.{K}", 45, K)
+    Wb = synth.q2k_matrix(5, f"prl.b.{K}", 19, K)
+    x = synth.bf16_normal(5, f"prl.x.{m}.{K}", (m, K))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    ya, yb = lib.q2k_mmvq_pair(dev(Wa), dev(Wb), xq, K)
+    assert torch.equal(ya, lib.q2k_mmvq_q8_1(dev(Wa), xq, K))
+    assert torch.equal(yb, lib.q2k_mmvq_q8_1(dev(Wb), xq, K))
+    xqf = oracle.q8_1_dequant(xq.cpu().numpy(), m, K)
+    for W, y in ((Wa, ya), (Wb, yb)):
+        refq = oracle.matvec(W, W.shape[0], K, xqf)
+        assert rel_err_rows(y.cpu().numpy(), refq) <= 1e-4
+        assert rel_err_rows(y.cpu().numpy(), oracle.matvec(W, W.shape[0], K, x_f64(x))) <= TOL_Q8
+
+
 # ---- a6: routed experts -------------------------------------------------------------
 
 @pytest.mark.parametrize("per_matrix", [False, True])
