@@ -119,15 +119,17 @@ int q2k_device_error(int32_t* host_out, int clear)
 {
     if (!host_out)
         return Q2K_ERR_NULL_ARG;
-    int32_t a = 0, b = 0, c = 0;
+    int32_t a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = mv_error_word(&a, clear != 0);
     if (e == cudaSuccess)
         e = gemm_error_word(&b, clear != 0);
     if (e == cudaSuccess)
         e = mt_error_word(&c, clear != 0);
+    if (e == cudaSuccess)
+        e = umma_error_word(&d, clear != 0);
     if (e != cudaSuccess)
         return fail_cuda(e);
-    *host_out = a | b | c;
+    *host_out = a | b | c | d;
     return Q2K_OK;
 }
 

@@ -196,6 +196,8 @@ cudaError_t launch_dense_gemm(const uint16_t* x, int64_t m, int64_t K, int64_t l
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
+    if (umma_supported(m, K, N))
+        return launch_dense_gemm_tc(x, m, K, ldx, W, N, y, ldy, s);  // tcgen05 / TMEM
     if (m <= 16)
         return launch_bt<16>(x, (int)m, (int)K, ldx, W, (int)N, y, ldy, di.sm_count, s);
     if (m <= 32)

@@ -52,10 +52,15 @@ cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void*
                                cudaStream_t s);
 cudaError_t launch_dense_gemm(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
                               int64_t N, float* y, int64_t ldy, cudaStream_t s);
+// The tcgen05 (tensor memory) GEMM for m >= 16 when the tensor-map encoder is there.
+bool umma_supported(int64_t m, int64_t K, int64_t N);
+cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
+                                 int64_t N, float* y, int64_t ldy, cudaStream_t s);
 
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
 cudaError_t gemm_error_word(int32_t* out, bool clear);
 cudaError_t mt_error_word(int32_t* out, bool clear);
+cudaError_t umma_error_word(int32_t* out, bool clear);
 
 }  // namespace q2k

@@ -361,13 +361,15 @@ def test_moe_m1_cfg3(lib, cfg3):
 
 # ---- a7: dense GEMM -----------------------------------------------------------------
 
-@pytest.mark.parametrize("m,N,K", [(1, 8, 16), (3, 65, 64), (16, 130, 200), (17, 64, 1024), (64, 256, 512),
-                                   (100, 70, 136), (256, 128, 256)])
-def test_dense_gemm_small(lib, m, N, K):
-    x = synth.bf16_normal(9, f"dg.x.{m}.{K}", (m, K))
+@pytest.mark.parametrize("m,N,K,pad", [(1, 8, 16, 0), (3, 65, 64, 0), (16, 130, 200, 0), (17, 64, 1024, 0),
+                                       (64, 256, 512, 0), (100, 70, 136, 0), (256, 128, 256, 0), (300, 200, 2048, 8),
+                                       (40, 1000, 4104, 0), (256, 384, 8192, 16)])
+def test_dense_gemm_small(lib, m, N, K, pad):
+    x = synth.bf16_normal(9, f"dg.x.{m}.{K}", (m, K + pad))
     W = synth.bf16_normal(9, f"dg.w.{N}.{K}", (N, K), std=0.02)
-    y = lib.dense_gemm_bf16(bf16_dev(x), bf16_dev(W)).cpu().numpy()
-    assert rel_err_rows(y, oracle.dense_gemm(x, W)) <= TOL_BF16
+    xd = bf16_dev(x)[:, :K]  # row stride K + pad
+    y = lib.dense_gemm_bf16(xd, bf16_dev(W)).cpu().numpy()
+    assert rel_err_rows(y, oracle.dense_gemm(np.ascontiguousarray(x[:, :K]), W)) <= TOL_BF16
 
 
 def test_engram_cfg1_rows_then_gemm(lib):
