@@ -46,43 +46,44 @@ __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow
 __host__ __device__ constexpr int log2_exact(int v) { return v <= 1 ? 0 : 1 + log2_exact(v / 2); }
 
 struct MvArgs {
+    // read by every thread in the prologue: kept together at the front
+    int rows_q, rows_r;  // rows_total = rows_q * grid + rows_r: CTA c owns rows_q (+1 if c < rows_r) rows
+    int rps;             // rows per stage = groups * RPT * sub
+    int nst;             // stages in the ring
+    uint32_t nst_magic;  // ceil(2^32 / nst): i / nst == umulhi(i, nst_magic) for i < 2^24
     int n_seg;
     int table;  // 1: W_table segments, stacked over one row range
-    const void* const* W_table;
-    const uint8_t* W[2];
     int N[2];
+    int x_bulk;     // 1: the first segment's activations arrive by bulk copy
+    int x_in_ring;  // 1: they arrive in the last ring slot, which the
+                    // weights take over once every warp holds its slice
+    int kb0;        // first block column of this K chunk
+    int nbc;        // blocks in this K chunk
+    int tc;         // threads
+    uint32_t rstride;  // shared-memory row stride (16-byte multiple)
+    uint32_t stage_bytes;
+    // shared-memory layout (byte offsets, each 16-byte aligned)
+    uint32_t off_x, off_bar, off_tab, off_cnt, off_red;
     int64_t row_bytes;  // bytes of a full weight row
-    int kb0;            // first block column of this K chunk
-    int nbc;            // blocks in this K chunk
     const uint8_t* x;
     int64_t x_tok_stride;
     int64_t x_seg_stride;
-    int x_align;  // 16, 4 or 2: widest copy the activation addresses allow
-    int x_bulk;   // 1: the first segment's activations arrive by bulk copy
-    int x_in_ring;  // 1: they arrive in the last ring slot, which the
-                    // weights take over once every warp holds its slice
+    const uint8_t* W[2];
+    const void* const* W_table;
+    // decomposition
+    int s_real;         // slices per row
+    int s_pad;          // lanes per row group
+    int groups;         // row groups
+    int sub;            // reduction units per stage
+    int rows_total;     // concat: N0 + N1; table: N
+    int max_stages;     // stages of the largest CTA
+    int x_align;        // 16, 4 or 2: widest copy the activation addresses allow
+    int accumulate;
     float* y[2];
     int64_t ldy[2];
     float* y_exp;
     const float* route_w;
     float* y_sum;
-    int accumulate;
-    // decomposition
-    int s_real;         // slices per row
-    int s_pad;          // lanes per row group
-    int groups;         // row groups
-    int tc;             // threads
-    int sub;            // reduction units per stage
-    int rps;            // rows per stage = groups * RPT * sub
-    int nst;            // stages in the ring
-    uint32_t nst_magic; // ceil(2^32 / nst): i / nst == umulhi(i, nst_magic) for i < 2^24
-    int rows_total;     // concat: N0 + N1; table: N
-    int rows_q, rows_r; // rows_total = rows_q * grid + rows_r: CTA c owns rows_q (+1 if c < rows_r) rows
-    int max_stages;     // stages of the largest CTA
-    uint32_t rstride;   // shared-memory row stride (16-byte multiple)
-    uint32_t stage_bytes;
-    // shared-memory layout (byte offsets, each 16-byte aligned)
-    uint32_t off_x, off_bar, off_tab, off_cnt, off_red;
 };
 
 struct Stage {
@@ -202,12 +203,20 @@ __device__ __forceinline__ void stage_x(const uint8_t* xseg, int64_t tok_stride,
 // 16-bit fixed point with one power-of-two exponent per group of 16 values
 // (the group of one Q2_K sub-block's codes in one bit plane).  The packed
 // words are stored word-major with an XOR swizzle, so the slice reads of a
-// warp (lanes 16 groups apart) fall in 32 different banks; the exponents
-// follow as one byte per group.
+// warp fall in 32 different banks (4-word slices: lanes 4 groups apart;
+// 8-word slices: lanes 8 groups apart); the exponents follow as one byte
+// per group.
 template <int M, int ACT, int SW>
-__host__ __device__ constexpr bool coop_x() { return ACT == ACT_BF16 && SW == 4 && M <= 2; }
+__host__ __device__ constexpr bool coop_x() { return ACT == ACT_BF16 && (SW == 4 || SW == 8) && M <= 2; }
 
-__device__ __forceinline__ int x_group_swz(int G) { return G ^ (((G >> 5) & 3) << 1); }
+template <int SW>
+__device__ __forceinline__ int x_group_swz(int G)
+{
+    if constexpr (SW == 8)
+        return G ^ ((G >> 5) & 7);
+    else
+        return G ^ (((G >> 5) & 3) << 1);
+}
 
 // Shared bytes the converted activations of m tokens take (words, then
 // exponent bytes).
@@ -215,7 +224,7 @@ __host__ __device__ constexpr int coop_x_bytes(int m, int nbc) { return m * nbc 
 
 constexpr int kCoopGroupsPerThread = 4;  // m * nbc * 16 <= 4 * threads (checked on the host)
 
-template <int M>
+template <int M, int SW>
 __device__ __forceinline__ void convert_x_bf16(uint8_t* xsm, int nbc)
 {
     const int NG = nbc * 16;  // groups of 16 values per token
@@ -266,7 +275,7 @@ __device__ __forceinline__ void convert_x_bf16(uint8_t* xsm, int nbc)
         const int q = threadIdx.x + k * blockDim.x;
         if (q < M * NG) {
             const int t = q / NG, G = q - t * NG;
-            uint32_t* wt = words + (size_t)t * NG * 8 + x_group_swz(G);
+            uint32_t* wt = words + (size_t)t * NG * 8 + x_group_swz<SW>(G);
 #pragma unroll
             for (int w = 0; w < 8; ++w)
                 wt[w * NG] = pk[k][w];
@@ -294,20 +303,24 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
             if constexpr (coop_x<M, ACT, SW>()) {
                 // converted words of group (b, n, j, h); the thread takes all 16 values
                 const int NG = nbc * 16;
-                const int G = b * 16 + 8 * n + 2 * j + (wi0 >> 2);
-                const uint32_t* wt = reinterpret_cast<const uint32_t*>(xsm) + (size_t)t * NG * 8 + x_group_swz(G);
-                const uint32_t eb = active ? (uint32_t)xsm[(size_t)M * NG * 32 + (size_t)t * NG + G] : 0u;
-                int sum = 0;
 #pragma unroll
-                for (int wl = 0; wl < 4; ++wl) {
-                    const uint32_t p0 = active ? wt[(2 * wl) * NG] : 0u;
-                    const uint32_t p1 = active ? wt[(2 * wl + 1) * NG] : 0u;
-                    sum = dp2a_lo_su(p0, 0x0101u, dp2a_lo_su(p1, 0x0101u, sum));
-                    sl.xa[t][j][wl][0] = p0;
-                    sl.xa[t][j][wl][1] = p1;
+                for (int hh = 0; hh < S::NH; ++hh) {
+                    const int G = b * 16 + 8 * n + 2 * j + (SW == 8 ? hh : (wi0 >> 2));
+                    const uint32_t* wt =
+                        reinterpret_cast<const uint32_t*>(xsm) + (size_t)t * NG * 8 + x_group_swz<SW>(G);
+                    const uint32_t eb = active ? (uint32_t)xsm[(size_t)M * NG * 32 + (size_t)t * NG + G] : 0u;
+                    int sum = 0;
+#pragma unroll
+                    for (int wl = 0; wl < 4; ++wl) {
+                        const uint32_t p0 = active ? wt[(2 * wl) * NG] : 0u;
+                        const uint32_t p1 = active ? wt[(2 * wl + 1) * NG] : 0u;
+                        sum = dp2a_lo_su(p0, 0x0101u, dp2a_lo_su(p1, 0x0101u, sum));
+                        sl.xa[t][j][hh * 4 + wl][0] = p0;
+                        sl.xa[t][j][hh * 4 + wl][1] = p1;
+                    }
+                    sl.xp[t][j][hh] = eb >= 27u ? __uint_as_float((eb - 14u - 2u * j) << 23) : 0.f;
+                    xsum[hh][j] = eb >= 27u ? (float)sum * __uint_as_float((eb - 14u) << 23) : 0.f;
                 }
-                sl.xp[t][j][0] = eb >= 27u ? __uint_as_float((eb - 14u - 2u * j) << 23) : 0.f;
-                xsum[0][j] = eb >= 27u ? (float)sum * __uint_as_float((eb - 14u) << 23) : 0.f;
             } else if constexpr (ACT == ACT_BF16) {
 #pragma unroll
                 for (int hh = 0; hh < S::NH; ++hh) {
@@ -501,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     // Read one field from every 32 bytes of the parameter block up front:
     // their first (cold) reads then overlap instead of queuing one after
     // another behind the dependent index arithmetic below.
-    asm volatile("" ::"r"(a.n_seg), "r"(a.N[0]), "l"(a.x_tok_stride), "l"(a.y[0]), "l"(a.y_exp), "r"(a.s_pad),
-                 "r"(a.rows_r), "r"(a.off_red));
+    asm volatile("" ::"r"(a.rows_q), "r"(a.x_bulk), "r"(a.off_x), "l"(a.x), "l"(a.W[1]), "r"(a.rows_total),
+                 "l"(a.ldy[0]), "l"(a.y_sum));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = a.tc >> 5;
@@ -715,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (warp > 0 && warp < pre)
             produce(warp);  // the rest of the prologue stages, now the activations are in
         if constexpr (coop_x<M, ACT, SW>())
-            convert_x_bf16<M>(xsm, a.nbc);  // every thread (the condition is uniform)
+            convert_x_bf16<M, SW>(xsm, a.nbc);  // every thread (the condition is uniform)
         load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         cur_e = tab[0].x;
         if (a.x_in_ring) {
@@ -741,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             stage_x<M, ACT>(a.x + (int64_t)st.e * a.x_seg_stride, a.x_tok_stride, a.kb0, a.nbc, a.x_align, xsm);
             __syncthreads();
             if constexpr (coop_x<M, ACT, SW>())
-                convert_x_bf16<M>(xsm, a.nbc);
+                convert_x_bf16<M, SW>(xsm, a.nbc);
             load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
         }
         cur_e = st.e;
@@ -904,8 +917,14 @@ cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
     return cudaGetLastError();
 }
 
-int sw_for(int act, int m)
+// Qs words per thread slice.  One token over a long row takes 8-word
+// slices (128 weights: the per-row scale, min and load work is spread over
+// twice the weights); short rows keep 4-word slices, so enough threads
+// share each row.
+int sw_for(int act, int m, int64_t nb)
 {
+    if (m == 1 && nb >= 32)
+        return 8;
     if (act == ACT_Q8)
         return m <= 4 ? 4 : 2;
     return m <= 2 ? 4 : (m <= 4 ? 2 : 1);
@@ -917,7 +936,7 @@ cudaError_t dispatch_m(int m, const MvArgs& a, int grid, size_t smem, cudaStream
     switch (m) {
 #define Q2K_CASE(MM)                                                                   \
     case MM:                                                                           \
-        if constexpr ((SW == 4 && (ACT == ACT_Q8 ? MM <= 4 : MM <= 2)) ||              \
+        if constexpr ((SW == 8 && MM == 1) || (SW == 4 && (ACT == ACT_Q8 ? MM <= 4 : MM <= 2)) || \
                       (SW == 2 && (ACT == ACT_Q8 ? MM >= 5 : (MM >= 3 && MM <= 4))) || \
                       (SW == 1 && ACT == ACT_BF16 && MM >= 5))                         \
             return launch_one<MM, ACT, SW>(a, grid, smem, s);                          \
@@ -930,6 +949,8 @@ cudaError_t dispatch_m(int m, const MvArgs& a, int grid, size_t smem, cudaStream
 
 cudaError_t dispatch(int act, int sw, int m, const MvArgs& a, int grid, size_t smem, cudaStream_t s)
 {
+    if (sw == 8)
+        return act == ACT_Q8 ? dispatch_m<ACT_Q8, 8>(m, a, grid, smem, s) : dispatch_m<ACT_BF16, 8>(m, a, grid, smem, s);
     if (act == ACT_Q8) {
         if (sw == 4)
             return dispatch_m<ACT_Q8, 4>(m, a, grid, smem, s);
@@ -960,7 +981,7 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         return cudaErrorInvalidValue;
 
     const int mc = p.m;  // the kernel family covers m <= 8 in one pass
-    const int sw = sw_for(p.act, mc);
+    const int sw = sw_for(p.act, mc, nb);
     const int spb = 16 / sw;
     const int rpt = rpt_for(mc);
     const int vp = pow2_ceil(rpt * mc);
@@ -1040,7 +1061,7 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         a.rows_r = (int)(a.rows_total % grid);
         const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
         a.max_stages = (int)stages_per_cta;
-        const bool coop = p.act == ACT_BF16 && sw == 4 && mc <= 2;
+        const bool coop = p.act == ACT_BF16 && (sw == 4 || sw == 8) && mc <= 2;
         if (coop && (int64_t)mc * nbc * 16 > (int64_t)kCoopGroupsPerThread * a.tc)
             return cudaErrorInvalidConfiguration;  // not reached: tc >= 4 * nbc and groups >= 2 for m = 2
         const size_t x_bytes = coop ? align16((size_t)coop_x_bytes(mc, nbc)) : align16((size_t)mc * nbc * xbpb);

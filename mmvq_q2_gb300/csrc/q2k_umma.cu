@@ -309,7 +309,8 @@ cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_
     a.atomic = splits > 1 ? 1 : 0;
     const size_t smem_cap = std::min<size_t>((size_t)di.smem_optin, 224 * 1024);
     const size_t fixed = 1024 + 64 + 16 * 8;
-    a.nst = (int)std::min<size_t>(8, (smem_cap - fixed) / a.stage_bytes);
+    const size_t cap2 = (gx * gy * splits > di.sm_count) ? std::min<size_t>(smem_cap, 112 * 1024) : smem_cap;
+    a.nst = (int)std::min<size_t>(8, (cap2 - fixed) / a.stage_bytes);
     if (a.nst < 2)
         return cudaErrorInvalidConfiguration;
     const size_t smem = fixed + (size_t)a.nst * a.stage_bytes;

@@ -363,7 +363,8 @@ def test_moe_m1_cfg3(lib, cfg3):
 
 @pytest.mark.parametrize("m,N,K,pad", [(1, 8, 16, 0), (3, 65, 64, 0), (16, 130, 200, 0), (17, 64, 1024, 0),
                                        (64, 256, 512, 0), (100, 70, 136, 0), (256, 128, 256, 0), (300, 200, 2048, 8),
-                                       (40, 1000, 4104, 0), (256, 384, 8192, 16)])
+                                       (40, 1000, 4104, 0), (256, 384, 8192, 16), (16, 4096, 128, 0),
+                                       (48, 2000, 320, 0), (600, 300, 192, 0)])
 def test_dense_gemm_small(lib, m, N, K, pad):
     x = synth.bf16_normal(9, f"dg.x.{m}.{K}", (m, K + pad))
     W = synth.bf16_normal(9, f"dg.w.{N}.{K}", (N, K), std=0.02)
