@@ -170,6 +170,33 @@ __device__ __forceinline__ void pack_sums(Slice<M, ACT, SW>& sl, int t, int hh, 
     sl.xsb[t][hh] = __uint_as_float((eb - 14u) << 23);
 }
 
+// 8-word slices: the eight group sums of a token, (j, h) for j = 0..3 and
+// h = 0, 1, as 16-bit fixed point with one power-of-two exponent, packed as
+// xs16[t][j >> 1][j & 1] = {sum(j, 0), sum(j, 1)}: the order of the min
+// nibbles in the two scale words of a half block.
+template <int M, int ACT, int SW>
+__device__ __forceinline__ void pack_sums8(Slice<M, ACT, SW>& sl, int t, const float (&xs)[2][4])
+{
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        amax = fmaxf(amax, fmaxf(fabsf(xs[0][j]), fabsf(xs[1][j])));
+    const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;
+    if (eb < 27u) {
+        sl.xs16[t][0][0] = sl.xs16[t][0][1] = sl.xs16[t][1][0] = sl.xs16[t][1][1] = 0u;
+        sl.xsb[t][0] = 0.f;
+        return;
+    }
+    const float scale = __uint_as_float((268u - eb) << 23);  // |xs * scale| < 2^15
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int q0 = __float2int_rn(xs[0][j] * scale);
+        const int q1 = __float2int_rn(xs[1][j] * scale);
+        sl.xs16[t][j >> 1][j & 1] = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16);
+    }
+    sl.xsb[t][0] = __uint_as_float((eb - 14u) << 23);
+}
+
 // Bytes of one token's activations per block column in the shared staging
 // region: 256 bf16 values, or 8 q8_1 blocks.
 template <int ACT>
@@ -233,38 +260,45 @@ __device__ __forceinline__ void convert_x_bf16(uint8_t* xsm, int nbc)
 #pragma unroll
     for (int k = 0; k < kCoopGroupsPerThread; ++k) {
         const int q = threadIdx.x + k * blockDim.x;
+        const bool valid = q < M * NG;  // M * NG is even: pairs are valid together
         ebv[k] = 0u;
 #pragma unroll
         for (int w = 0; w < 8; ++w)
             pk[k][w] = 0u;
-        if (q < M * NG) {
+        float v[16];
+        float amax = 0.f;
+        if (valid) {
             const uint8_t* src = xsm + (size_t)q * 32;  // token-major, 32 bytes per group
             const uint4 u0 = *reinterpret_cast<const uint4*>(src);
             const uint4 u1 = *reinterpret_cast<const uint4*>(src + 16);
             const uint32_t raw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            float v[16];
-            float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 v[2 * i] = __uint_as_float(raw[i] << 16);
                 v[2 * i + 1] = __uint_as_float(raw[i] & 0xFFFF0000u);
                 amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
             }
-            const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;  // biased exponent of amax
-            if (eb >= 27u) {
-                // x16 = x * 2^(141-eb): |x16| < 2^15, exact for the group's
-                // largest 2^8 range.  Adding 1.5*2^23 (ulp 1) rounds to the
-                // nearest integer, ties to even, and leaves it in the low
-                // mantissa bits as a 16-bit two's complement value.
-                const float scale = __uint_as_float((268u - eb) << 23);
+        }
+        uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;  // biased exponent of amax
+        if constexpr (SW == 8) {
+            // 8-word slices: the two groups of a 32-value pair (one q8_1-sized
+            // block) share the larger exponent (the partner is lane ^ 1)
+            eb = max(eb, (uint32_t)__shfl_xor_sync(0xffffffffu, (int)eb, 1));
+        }
+        if (valid && eb >= 27u) {
+            // x16 = x * 2^(XS-eb): |x16| < 2^15 (4-word slices, XS = 141) or
+            // 2^14 (8-word slices, XS = 140, so that two sub-block sums add in
+            // int32), exact for the group's largest 2^8 range.  Adding 1.5*2^23
+            // (ulp 1) rounds to the nearest integer, ties to even, and leaves
+            // it in the low mantissa bits as a 16-bit two's complement value.
+            const float scale = __uint_as_float(((SW == 8 ? 267u : 268u) - eb) << 23);
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const uint32_t f0 = __float_as_uint(fmaf(v[2 * w], scale, 12582912.0f));
-                    const uint32_t f1 = __float_as_uint(fmaf(v[2 * w + 1], scale, 12582912.0f));
-                    pk[k][w] = __byte_perm(f0, f1, 0x5410u);
-                }
-                ebv[k] = eb;
+            for (int w = 0; w < 8; ++w) {
+                const uint32_t f0 = __float_as_uint(fmaf(v[2 * w], scale, 12582912.0f));
+                const uint32_t f1 = __float_as_uint(fmaf(v[2 * w + 1], scale, 12582912.0f));
+                pk[k][w] = __byte_perm(f0, f1, 0x5410u);
             }
+            ebv[k] = eb;
         }
     }
     __syncthreads();  // every group has been read before any is overwritten
@@ -318,8 +352,9 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
                         sl.xa[t][j][hh * 4 + wl][0] = p0;
                         sl.xa[t][j][hh * 4 + wl][1] = p1;
                     }
-                    sl.xp[t][j][hh] = eb >= 27u ? __uint_as_float((eb - 14u - 2u * j) << 23) : 0.f;
-                    xsum[hh][j] = eb >= 27u ? (float)sum * __uint_as_float((eb - 14u) << 23) : 0.f;
+                    constexpr uint32_t XO = SW == 8 ? 13u : 14u;  // x16 = x * 2^(127 + XO - eb)
+                    sl.xp[t][j][hh] = eb >= 27u ? __uint_as_float((eb - XO - 2u * j) << 23) : 0.f;
+                    xsum[hh][j] = eb >= 27u ? (float)sum * __uint_as_float((eb - XO) << 23) : 0.f;
                 }
             } else if constexpr (ACT == ACT_BF16) {
 #pragma unroll
@@ -403,9 +438,13 @@ __device__ __forceinline__ void load_slice(Slice<M, ACT, SW>& sl, const uint8_t*
                 }
             }
         }
+        if constexpr (SW == 8) {
+            pack_sums8<M, ACT, SW>(sl, t, xsum);
+        } else {
 #pragma unroll
-        for (int hh = 0; hh < S::NH; ++hh)
-            pack_sums<M, ACT, SW>(sl, t, hh, xsum[hh]);
+            for (int hh = 0; hh < S::NH; ++hh)
+                pack_sums<M, ACT, SW>(sl, t, hh, xsum[hh]);
+        }
     }
 }
 
@@ -425,40 +464,82 @@ __device__ __forceinline__ void slice_dot(const Slice<M, ACT, SW>& sl, const uin
     const uint32_t dm = lds32(blk + 80);
     const float d = half_lo_f(dm);
     const float dmin = half_hi_f(dm);
-#pragma unroll
-    for (int hh = 0; hh < S::NH; ++hh) {
-        const uint32_t h = (SW == 8) ? (uint32_t)hh : (uint32_t)(wi0 >> 2);
-        // scale bytes of sub-blocks 8n + 2j + h, j = 0..3
-        const uint32_t sb = __byte_perm(s0, s1, h | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12));
-        const uint32_t scn = sb & 0x0F0F0F0Fu;
-        const uint32_t mnn = (sb >> 4) & 0x0F0F0F0Fu;
-        // scale nibbles as integers: the sub-block sum is scaled in int32
-        // (|S| * 15 < 2^31) before its one conversion to float
-        const int sci[4] = {(int)__byte_perm(scn, 0u, 0x4440u), (int)__byte_perm(scn, 0u, 0x4441u),
-                            (int)__byte_perm(scn, 0u, 0x4442u), (int)__byte_perm(scn, 0u, 0x4443u)};
+    if constexpr (SW == 8) {
+        // A whole half block: sub-block 8n + 2j + h has its scale byte at
+        // 2j + h of the two scale words.  The two halves h of bit plane j
+        // share one activation scale, so their sums meet in int32
+        // (|S| * 15 * 2 < 2^31) before the one conversion to float.
+        const uint32_t scn[2] = {s0 & 0x0F0F0F0Fu, s1 & 0x0F0F0F0Fu};
+        const uint32_t mnn[2] = {(s0 >> 4) & 0x0F0F0F0Fu, (s1 >> 4) & 0x0F0F0F0Fu};
 #pragma unroll
         for (int t = 0; t < M; ++t) {
-            // min term: sum_j m_j * xsum_j as two 16x8-bit dot products
-            const int Bi = dp2a_hi_su(sl.xs16[t][hh][1], mnn, dp2a_lo_su(sl.xs16[t][hh][0], mnn, 0));
-            const float B = sl.xsb[t][hh] * (float)Bi;
+            // min term: the eight group sums against the eight min nibbles
+            int Bi = dp2a_lo_su(sl.xs16[t][0][0], mnn[0], 0);
+            Bi = dp2a_hi_su(sl.xs16[t][0][1], mnn[0], Bi);
+            Bi = dp2a_lo_su(sl.xs16[t][1][0], mnn[1], Bi);
+            Bi = dp2a_hi_su(sl.xs16[t][1][1], mnn[1], Bi);
             float A = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                int Sacc = 0;
+                int Sh[2];
 #pragma unroll
-                for (int wl = 0; wl < S::WPH; ++wl) {
-                    const int w = hh * S::WPH + wl;
-                    const uint32_t c = qw[w] & (0x03030303u << (2 * j));
-                    if constexpr (ACT == ACT_BF16) {
-                        Sacc = dp2a_lo_su(sl.xa[t][j][w][0], c, Sacc);
-                        Sacc = dp2a_hi_su(sl.xa[t][j][w][1], c, Sacc);
-                    } else {
-                        Sacc = dp4a_us(c, sl.xa[t][j][w][0], Sacc);
+                for (int hh = 0; hh < 2; ++hh) {
+                    int Sacc = 0;
+#pragma unroll
+                    for (int wl = 0; wl < 4; ++wl) {
+                        const int w = hh * 4 + wl;
+                        const uint32_t c = qw[w] & (0x03030303u << (2 * j));
+                        if constexpr (ACT == ACT_BF16) {
+                            Sacc = dp2a_lo_su(sl.xa[t][j][w][0], c, Sacc);
+                            Sacc = dp2a_hi_su(sl.xa[t][j][w][1], c, Sacc);
+                        } else {
+                            Sacc = dp4a_us(c, sl.xa[t][j][w][0], Sacc);
+                        }
                     }
+                    Sh[hh] = Sacc;
                 }
-                A = fmaf(sl.xp[t][j][hh], (float)(Sacc * sci[j]), A);
+                const int sc0 = (int)__byte_perm(scn[j >> 1], 0u, 0x4440u | (uint32_t)((2 * j) & 3));
+                const int sc1 = (int)__byte_perm(scn[j >> 1], 0u, 0x4440u | (uint32_t)((2 * j + 1) & 3));
+                A = fmaf(sl.xp[t][j][0], (float)(Sh[0] * sc0 + Sh[1] * sc1), A);
             }
-            acc[t] = fmaf(d, A, fmaf(-dmin, B, acc[t]));
+            acc[t] = fmaf(d, A, fmaf(-dmin, sl.xsb[t][0] * (float)Bi, acc[t]));
+        }
+    } else {
+#pragma unroll
+        for (int hh = 0; hh < S::NH; ++hh) {
+            const uint32_t h = (SW == 8) ? (uint32_t)hh : (uint32_t)(wi0 >> 2);
+            // scale bytes of sub-blocks 8n + 2j + h, j = 0..3
+            const uint32_t sb = __byte_perm(s0, s1, h | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12));
+            const uint32_t scn = sb & 0x0F0F0F0Fu;
+            const uint32_t mnn = (sb >> 4) & 0x0F0F0F0Fu;
+            // scale nibbles as integers: the sub-block sum is scaled in int32
+            // (|S| * 15 < 2^31) before its one conversion to float
+            const int sci[4] = {(int)__byte_perm(scn, 0u, 0x4440u), (int)__byte_perm(scn, 0u, 0x4441u),
+                                (int)__byte_perm(scn, 0u, 0x4442u), (int)__byte_perm(scn, 0u, 0x4443u)};
+#pragma unroll
+            for (int t = 0; t < M; ++t) {
+                // min term: sum_j m_j * xsum_j as two 16x8-bit dot products
+                const int Bi = dp2a_hi_su(sl.xs16[t][hh][1], mnn, dp2a_lo_su(sl.xs16[t][hh][0], mnn, 0));
+                const float B = sl.xsb[t][hh] * (float)Bi;
+                float A = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    int Sacc = 0;
+#pragma unroll
+                    for (int wl = 0; wl < S::WPH; ++wl) {
+                        const int w = hh * S::WPH + wl;
+                        const uint32_t c = qw[w] & (0x03030303u << (2 * j));
+                        if constexpr (ACT == ACT_BF16) {
+                            Sacc = dp2a_lo_su(sl.xa[t][j][w][0], c, Sacc);
+                            Sacc = dp2a_hi_su(sl.xa[t][j][w][1], c, Sacc);
+                        } else {
+                            Sacc = dp4a_us(c, sl.xa[t][j][w][0], Sacc);
+                        }
+                    }
+                    A = fmaf(sl.xp[t][j][hh], (float)(Sacc * sci[j]), A);
+                }
+                acc[t] = fmaf(d, A, fmaf(-dmin, B, acc[t]));
+            }
         }
     }
 }
