@@ -205,4 +205,29 @@ __device__ __forceinline__ float bf16_bits_f(uint16_t b)
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched as
+// a programmatic dependent of the previous kernel in its stream, so its
+// launch and setup overlap that kernel's tail.  A kernel lets its own
+// dependents be scheduled at entry and calls pdl_wait() before its first
+// access to global memory (the previous grid may still be writing it); the
+// wait returns at once when the kernel was launched normally.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace q2k

@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(128) dense_gemm_kernel(const uint16_t* __restr
     constexpr int STAGE = W_BYTES + X_BYTES;
     constexpr int NT = BT / 8;  // n8 tiles per warp
 
+    pdl_launch_dependents();
+    pdl_wait();
     const int n0 = blockIdx.x * kBN;
     const int t0 = blockIdx.y * BT;
     const int kbeg = blockIdx.z * k_per_split;
@@ -183,8 +185,8 @@ cudaError_t launch_bt(const uint16_t* x, int m, int K, int64_t ldx, const uint16
             return e;
     }
     dim3 grid(gx, gy, splits);
-    dense_gemm_kernel<BT><<<grid, 128, SMEM, s>>>(x, m, K, ldx, W, N, y, ldy, kps, splits > 1 ? 1 : 0);
-    return cudaGetLastError();
+    return launch_pdl(dense_gemm_kernel<BT>, grid, dim3(128), (size_t)SMEM, s, x, m, K, ldx, W, N, y, ldy, kps,
+                      splits > 1 ? 1 : 0);
 }
 
 }  // namespace

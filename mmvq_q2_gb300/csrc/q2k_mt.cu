@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     q2k_mt_kernel(const MtArgs a, const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();  // the next kernel may set itself up meanwhile
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, cq = lane & 3;  // MMA fragment row group and column pair
@@ -367,6 +368,8 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     }
     for (int i = tid; i < a.yacc_rows * a.ychunks * kTok; i += blockDim.x)
         yacc[i] = 0.f;
+    // global memory may still be written by the previous kernel in the stream
+    pdl_wait();
     __syncthreads();
 
     // ---- producer role: stage j (K chunk, tile group) into its ring slot.
@@ -699,8 +702,7 @@ cudaError_t launch_mt_one(const MtArgs& a, const CUtensorMap& tm0, const CUtenso
         configured_for = dev;
         configured_smem = smem;
     }
-    k<<<grid, kMtThreads, smem, s>>>(a, tm0, tm1);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3((unsigned)grid), dim3(kMtThreads), smem, s, a, tm0, tm1);
 }
 
 }  // namespace

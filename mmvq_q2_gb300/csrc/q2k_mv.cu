@@ -597,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     // another behind the dependent index arithmetic below.
     asm volatile("" ::"r"(a.rows_q), "r"(a.x_bulk), "r"(a.off_x), "l"(a.x), "l"(a.W[1]), "r"(a.rows_total),
                  "l"(a.ldy[0]), "l"(a.y_sum));
+    pdl_launch_dependents();  // the next kernel may set itself up meanwhile
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = a.tc >> 5;
@@ -672,6 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             mbar_init(smem_u32(&full_b[s]), 1);
         fence_mbar_init();
     }
+    // Everything above reads only parameters and shared memory; global
+    // memory may still be written by the previous kernel in the stream.
+    pdl_wait();
     if (tid == 0) {
         if (x_first_bulk) {
             // the activations first, ahead of the weight prefetch
@@ -994,8 +998,7 @@ cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
         configured_for = dev;
         configured_smem = smem;
     }
-    k<<<grid, a.tc, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3((unsigned)grid), dim3((unsigned)a.tc), smem, s, a);
 }
 
 // Qs words per thread slice.  One token over a long row takes 8-word

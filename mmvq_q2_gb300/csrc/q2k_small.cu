@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) q2k_dequant_kernel(const uint8_t* __restr
                                                           int nb, const int32_t* __restrict__ ids, int64_t n_rows,
                                                           uint16_t* __restrict__ out, int32_t* err_flag)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t total = n_rows * nb * 32;
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
         const int l = (int)(u & 31);
@@ -78,13 +80,12 @@ cudaError_t launch_dequant_rows(const void* table, int64_t n_table_rows, int64_t
     const int64_t threads = n_rows * nb * 32;
     const int64_t grid = std::min<int64_t>((threads + 255) / 256, (int64_t)di.sm_count * 8);
     const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    const uint8_t* tb = static_cast<const uint8_t*>(table);
     if (vec)
-        q2k_dequant_kernel<true><<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t*>(table), n_table_rows, nb,
-                                                            ids, n_rows, out, err_flag);
-    else
-        q2k_dequant_kernel<false><<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t*>(table), n_table_rows, nb,
-                                                             ids, n_rows, out, err_flag);
-    return cudaGetLastError();
+        return launch_pdl(q2k_dequant_kernel<true>, dim3((unsigned)grid), dim3(256), 0, s, tb, n_table_rows, nb, ids,
+                          n_rows, out, err_flag);
+    return launch_pdl(q2k_dequant_kernel<false>, dim3((unsigned)grid), dim3(256), 0, s, tb, n_table_rows, nb, ids,
+                      n_rows, out, err_flag);
 }
 
 // ---- q8_1 ---------------------------------------------------------------------
@@ -125,6 +126,8 @@ __device__ __forceinline__ void q8_1_encode_group(const float (&v)[4], uint8_t* 
 __global__ void __launch_bounds__(256) q8_1_quantize_kernel(const uint16_t* __restrict__ x, int64_t m, int nblk,
                                                             int64_t ldx, uint8_t* __restrict__ out)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t total = m * nblk * 8;  // lanes
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     // every lane of a warp must reach the shuffles: iterate a warp-uniform count
@@ -155,14 +158,16 @@ cudaError_t launch_q8_1_quantize(const uint16_t* x, int64_t m, int64_t K, int64_
     const int nblk = (int)(K / kQ8Values);
     const int64_t lanes = m * nblk * 8;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((lanes + 255) / 256, (int64_t)di.sm_count * 8));
-    q8_1_quantize_kernel<<<(int)grid, 256, 0, s>>>(x, m, nblk, ldx, static_cast<uint8_t*>(out));
-    return cudaGetLastError();
+    return launch_pdl(q8_1_quantize_kernel, dim3((unsigned)grid), dim3(256), 0, s, x, m, nblk, ldx,
+                      static_cast<uint8_t*>(out));
 }
 
 // ---- SwiGLU + q8_1 --------------------------------------------------------------
 __global__ void __launch_bounds__(256) swiglu_q8_1_kernel(const float* __restrict__ gate_up, int64_t E, int64_t N,
                                                           uint8_t* __restrict__ h_q8, uint16_t* __restrict__ h_bf16)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int nblk = (int)(N / kQ8Values);
     const int64_t total = E * nblk * 8;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -206,8 +211,8 @@ cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void*
         return e;
     const int64_t lanes = E * (N / kQ8Values) * 8;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((lanes + 255) / 256, (int64_t)di.sm_count * 8));
-    swiglu_q8_1_kernel<<<(int)grid, 256, 0, s>>>(gate_up, E, N, static_cast<uint8_t*>(h_q8), h_bf16);
-    return cudaGetLastError();
+    return launch_pdl(swiglu_q8_1_kernel, dim3((unsigned)grid), dim3(256), 0, s, gate_up, E, N,
+                      static_cast<uint8_t*>(h_q8), h_bf16);
 }
 
 }  // namespace q2k

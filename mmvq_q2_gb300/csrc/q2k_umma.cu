@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     umma_gemm_kernel(const UmArgs a, const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    pdl_launch_dependents();  // the next kernel may set itself up meanwhile
     // the 128-byte swizzle repeats every 1024 bytes: stages start on 1024
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,6 +150,8 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // global memory may still be written by the previous kernel in the stream
+    pdl_wait();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -332,8 +335,7 @@ cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_
         if (e != cudaSuccess)
             return e;
     }
-    umma_gemm_kernel<<<dim3(gx, gy, splits), kUmThreads, smem, s>>>(a, tw, tx);
-    return cudaGetLastError();
+    return launch_pdl(umma_gemm_kernel, dim3(gx, gy, splits), dim3(kUmThreads), smem, s, a, tw, tx);
 }
 
 cudaError_t umma_error_word(int32_t* out, bool clear)
