@@ -17,9 +17,11 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   and x from pinned host memory, calls the C ABI, and reads y back.
 * cpu_baseline times the CPU oracle (one thread) on a bounded sample.
 * --impl reference times the CPU oracle on the same workload (rank 0 only).
-* --ncu-case runs a few untimed calls of the headline kernel (bf16 GEMV) and
-  of the q8_1 MMVQ on the headline shape, for a profiler capture; it prints
-  no JSON line.
+* --ncu-case [mv|mt|gemm] runs a few untimed calls for a profiler capture
+  and prints no JSON line: mv = the headline kernel (bf16 GEMV) and the q8_1
+  MMVQ at m=1 on the headline shape; mt = the same shape at m=8 (the
+  tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
+  N=K=16384.
 * --all also times every configuration of the sweep and prints one JSON
   object per configuration to stderr (and to gpurun_out/bench_all.jsonl when
   that folder exists).
@@ -518,23 +520,34 @@ def run_reference(args):
     }
 
 
-def run_ncu_case(calls: int = 3):
-    """A small fixed workload for a profiler: `calls` eager calls of
+def run_ncu_case(which: str = "mv", calls: int = 3):
+    """A small fixed workload for a profiler (the profiler flushes the caches
+    between passes; one weight copy).  mv: `calls` eager calls of
     q2k_gemv_bf16, then of q2k_mmvq_q8_1, at m=1 N=K=16384 (88 MB of
-    weights, one copy; the profiler flushes the caches between passes)."""
+    weights).  mt: the same at m=8.  gemm: dense_gemm_bf16 at m=64, then
+    m=256, N=K=16384 (537 MB of bf16 weights), one call each."""
     import torch
     from mmvq_q2_gb300 import build as b
     b.build()
     import mmvq_q2_gb300 as q
-    W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
-    x = synth.bf16_normal(0, "sweep.x1", (1, K_HEAD))
-    Wd = torch.from_numpy(W).cuda()
-    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
-    xq = q.q8_1_quantize_rows(xd)
-    for _ in range(calls):
-        q.q2k_gemv_bf16(Wd, xd)
-    for _ in range(calls):
-        q.q2k_mmvq_q8_1(Wd, xq, K_HEAD)
+    if which == "gemm":
+        W = synth.bf16_normal(0, "sweep.dense.W", (N_HEAD, K_HEAD), std=0.02)
+        Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+        for m in (64, 256):
+            x = synth.bf16_normal(0, f"sweep.dense.x{m}", (m, K_HEAD))
+            xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+            q.dense_gemm_bf16(xd, Wd)
+    else:
+        m = 8 if which == "mt" else 1
+        W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
+        x = synth.bf16_normal(0, f"sweep.x{m}", (m, K_HEAD))
+        Wd = torch.from_numpy(W).cuda()
+        xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        xq = q.q8_1_quantize_rows(xd)
+        for _ in range(calls):
+            q.q2k_gemv_bf16(Wd, xd)
+        for _ in range(calls):
+            q.q2k_mmvq_q8_1(Wd, xq, K_HEAD)
     torch.cuda.synchronize()
     print("ncu case done", file=sys.stderr)
 
@@ -546,10 +559,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
-    ap.add_argument("--ncu-case", action="store_true")
+    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
-        run_ncu_case()
+        run_ncu_case(args.ncu_case)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
