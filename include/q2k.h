@@ -134,7 +134,13 @@ int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t
  *                equals q2k_mmvq_q8_1(W_table[e], xq row) bit for bit
  *   route_w      fp32 [n_mat], required with y_sum
  *   y_sum        fp32 [N], nullable: y_sum[n] = sum_e route_w[e]*y[e,n],
- *                added in e order (deterministic)
+ *                added in e order (deterministic).  With per-matrix
+ *                inputs and y given, each matrix gets CTAs of its own and
+ *                the sum is a second launch over y; the bits are the same.
+ *                Without y the sum is fused: each CTA keeps the partial
+ *                sums of all n_mat matrices for its rows in shared memory,
+ *                and a problem whose partials do not fit fails with a CUDA
+ *                configuration error (pass y for many small matrices).
  * Gate and up run as one batch of 2*topk matrices; down as topk matrices
  * with x_per_matrix = 1 (moe_v41/init.rs, the `gate_out` comment). */
 int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K,
@@ -156,15 +162,16 @@ int swiglu_q8_1_rows(const float* gate_up, int64_t E, int64_t N, void* h_q8, uin
 size_t q2k_moe_m1_workspace_bytes(int64_t E, int64_t dim, int64_t inter);
 
 /* The routed-expert step for one token as one call (moe_v41/init.rs): q8_1
- * of x, the 2E gate+up batch, SwiGLU + q8_1 of h, the E down batch with
- * the route-weighted sum.  Four launches on `stream`.
+ * of x, the 2E gate+up batch, SwiGLU + q8_1 of h, the E down batch, the
+ * route-weighted sum.  Five launches on `stream`.
  *   ptrs      device array of 3E device pointers: gate_0..gate_{E-1}
  *             ([inter, dim] each), up_0..up_{E-1} ([inter, dim]),
  *             down_0..down_{E-1} ([dim, inter]) (moe_v41/init.rs, `ptrs_dev`)
  *   x_bf16    [dim];  route_w fp32 [E];  y fp32 [dim]
  *   workspace at least q2k_moe_m1_workspace_bytes(E, dim, inter) bytes,
  *             256-byte aligned; its contents on return are the q8_1 x, the
- *             fp32 gate/up outputs and the q8_1 h, in that order. */
+ *             fp32 gate/up outputs, the q8_1 h and the fp32 down outputs
+ *             [E, dim] (before the route weights), in that order. */
 int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
                const uint16_t* x_bf16, const float* route_w, float* y, void* workspace,
                size_t workspace_bytes, q2k_stream_t stream);
@@ -181,7 +188,7 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
  * in the library's device image; nothing is allocated or freed.  Problems
  * with q2k_moe_m1_workspace_bytes(E, dim, inter) above that size return
  * Q2K_ERR_WORKSPACE before anything is enqueued (E = 8, dim = 4096,
- * inter = 2048 needs 154,112 bytes).  The first call on each device looks
+ * inter = 2048 needs 285,184 bytes).  The first call on each device looks
  * the scratch's address up (cudaGetSymbolAddress, which may load the
  * module); make that first call before any stream capture.  Calls that
  * overlap on one device share the scratch and race: issue them on one

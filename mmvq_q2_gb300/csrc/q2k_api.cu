@@ -279,7 +279,18 @@ int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64
     p.x = xq;
     p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
     p.x_seg_stride = x_per_matrix ? (int64_t)q8_1_row_bytes(K) : 0;
-    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (x_per_matrix && y && y_sum) {
+        // one matrix per CTA (its input row staged once), then the
+        // route-weighted sum over the outputs y in a second pass
+        p.seg_major = 1;
+        p.y_sum = nullptr;
+        cudaError_t e = launch_mv(p, s);
+        if (e != cudaSuccess)
+            return fail_cuda(e);
+        return finish(launch_expert_sum(y, route_w, n_mat, N, y_sum, s));
+    }
+    return finish(launch_mv(p, s));
 }
 
 int swiglu_q8_1_rows(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16, q2k_stream_t stream)
@@ -303,7 +314,7 @@ size_t q2k_moe_m1_workspace_bytes(int64_t E, int64_t dim, int64_t inter)
     if (E <= 0 || dim <= 0 || inter <= 0 || dim % kBlockWeights || inter % kBlockWeights)
         return 0;
     return round256(q8_1_row_bytes(dim)) + round256((size_t)2 * E * inter * sizeof(float)) +
-           round256((size_t)E * q8_1_row_bytes(inter));
+           round256((size_t)E * q8_1_row_bytes(inter)) + round256((size_t)E * dim * sizeof(float));
 }
 
 int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, const uint16_t* x_bf16,
@@ -327,6 +338,7 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     void* xq = ws;
     float* gate_up = reinterpret_cast<float*>(ws + round256(q8_1_row_bytes(dim)));
     void* h_q8 = ws + round256(q8_1_row_bytes(dim)) + round256((size_t)2 * E * inter * sizeof(float));
+    float* down_out = reinterpret_cast<float*>(static_cast<uint8_t*>(h_q8) + round256((size_t)E * q8_1_row_bytes(inter)));
     cudaError_t e = launch_q8_1_quantize(x_bf16, 1, dim, dim, xq, s);
     if (e != cudaSuccess)
         return fail_cuda(e);
@@ -352,13 +364,14 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     d.n_seg = (int)E;
     d.W_table = ptrs + 2 * E;
     d.N[0] = dim;
-    d.y_exp = nullptr;
-    d.route_w = route_w;
-    d.y_sum = y;
+    d.y_exp = down_out;  // one expert per CTA, then the route-weighted sum
+    d.seg_major = 1;
     d.x = h_q8;
     d.x_tok_stride = (int64_t)q8_1_row_bytes(inter);
     d.x_seg_stride = (int64_t)q8_1_row_bytes(inter);
-    return finish(launch_mv(d, s));
+    if ((e = launch_mv(d, s)) != cudaSuccess)
+        return fail_cuda(e);
+    return finish(launch_expert_sum(down_out, route_w, E, dim, y, s));
 }
 
 int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W, int64_t N, float* y,

@@ -37,6 +37,8 @@ struct MvProblem {
     const void* x;           // bf16 elements or q8_1 bytes
     int64_t x_tok_stride;    // bytes between tokens
     int64_t x_seg_stride;    // bytes between segments' inputs (0 = shared)
+    int seg_major;           // table, per-segment inputs, no y_sum: each CTA
+                             // works on one segment (its input staged once)
 };
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
@@ -50,6 +52,9 @@ cudaError_t launch_q8_1_quantize(const uint16_t* x, int64_t m, int64_t K, int64_
                                  cudaStream_t s);
 cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16,
                                cudaStream_t s);
+// y_sum[n] = sum_e route_w[e] * y_exp[e][n], fp32 fmaf in e order from 0.
+cudaError_t launch_expert_sum(const float* y_exp, const float* route_w, int64_t E, int64_t N, float* y_sum,
+                              cudaStream_t s);
 cudaError_t launch_dense_gemm(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
                               int64_t N, float* y, int64_t ldy, cudaStream_t s);
 // The tcgen05 (tensor memory) GEMM for m >= 16 when the tensor-map encoder is there.

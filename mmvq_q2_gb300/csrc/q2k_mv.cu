@@ -52,7 +52,10 @@ struct MvArgs {
     int nst;             // stages in the ring
     uint32_t nst_magic;  // ceil(2^32 / nst): i / nst == umulhi(i, nst_magic) for i < 2^24
     int n_seg;
-    int table;  // 1: W_table segments, stacked over one row range
+    int table;      // 1: W_table segments, stacked over one row range
+    int seg_major;  // table only: CTA c works on segment c / cps alone, rows
+                    // split cps ways (per-segment activations staged once)
+    int cps;        // CTAs per segment (seg_major)
     int N[2];
     int x_bulk;     // 1: the first segment's activations arrive by bulk copy
     int x_in_ring;  // 1: they arrive in the last ring slot, which the
@@ -97,7 +100,7 @@ __device__ __forceinline__ int stage_count(const MvArgs& a, int lo, int hi)
     if (hi <= lo)
         return 0;
     if (a.table)
-        return ((hi - lo + a.rps - 1) / a.rps) * a.n_seg;
+        return ((hi - lo + a.rps - 1) / a.rps) * (a.seg_major ? 1 : a.n_seg);
     const int n0 = a.N[0];
     const int l0 = max(0, min(hi, n0) - lo);
     const int l1 = max(0, hi - max(lo, n0));
@@ -105,11 +108,16 @@ __device__ __forceinline__ int stage_count(const MvArgs& a, int lo, int hi)
 }
 
 // Stage i of the CTA owning rows [lo, hi): the rows split at the segment
-// end (concat: both matrices' rows one after the other) or repeated for
-// every segment (table), in chunks of rps rows.
-__device__ __forceinline__ Stage stage_at(const MvArgs& a, int lo, int hi, int i)
+// end (concat: both matrices' rows one after the other), repeated for every
+// segment (table), or of the CTA's one segment seg (table, seg_major), in
+// chunks of rps rows.
+__device__ __forceinline__ Stage stage_at(const MvArgs& a, int lo, int hi, int i, int seg)
 {
     if (a.table) {
+        if (a.seg_major) {
+            const int r = lo + i * a.rps;
+            return Stage{seg, r, min(a.rps, hi - r)};
+        }
         const int per = (hi - lo + a.rps - 1) / a.rps;
         const int e = i / per, c = i - e * per;
         const int r = lo + c * a.rps;
@@ -620,7 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     int* next_issue = cnt + a.nst + 1;  // the next stage to copy in
     float* red = reinterpret_cast<float*>(smem + a.off_red);
 
-    const int cta = blockIdx.x;
+    // seg_major: CTAs [e * cps, (e + 1) * cps) split the rows of segment e
+    const int seg = a.seg_major ? (int)blockIdx.x / a.cps : 0;
+    const int cta = (int)blockIdx.x - seg * (a.seg_major ? a.cps : 0);
     const int lo = cta * a.rows_q + min(cta, a.rows_r);
     const int hi = lo + a.rows_q + (cta < a.rows_r ? 1 : 0);
     const int nstages = stage_count(a, lo, hi);
@@ -679,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     if (tid == 0) {
         if (x_first_bulk) {
             // the activations first, ahead of the weight prefetch
-            const int e0 = stage_at(a, lo, hi, 0).e;
+            const int e0 = stage_at(a, lo, hi, 0, seg).e;
             const uint8_t* xs0 = a.x + (int64_t)e0 * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
             const uint64_t pol = l2_policy_evict_last();  // every CTA reads them
             mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
@@ -693,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     // copy engine serves the bytes needed first, first.
     const bool issue_now = warp < pre && (warp == 0 || !x_first_bulk);
     if (issue_now) {
-        const Stage st0 = stage_at(a, lo, hi, warp);
+        const Stage st0 = stage_at(a, lo, hi, warp, seg);
         const int4 st = make_int4(st0.e, st0.row0, st0.nrows, 0);
         const uint8_t* src0 = stage_src(st);
         early = src_aligned(src0);  // uniform within the warp
@@ -701,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             copy_stage(warp, st, src0);
     }
     for (int i = tid; i < nstages; i += blockDim.x) {
-        const Stage st = stage_at(a, lo, hi, i);
+        const Stage st = stage_at(a, lo, hi, i, seg);
         tab[i] = make_int4(st.e, st.row0, st.nrows, 0);
     }
     __syncthreads();
@@ -1127,30 +1137,41 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
 
         a.rows_total = table ? (int)p.N[0] : (int)(p.N[0] + (p.n_seg > 1 ? p.N[1] : 0));
         const int wpg = a.s_pad >= 32 ? a.s_pad / 32 : 1;
-        int64_t grid = std::min<int64_t>(di.sm_count, std::max<int64_t>(1, a.rows_total / 2));
-        int64_t rows_per_cta = (a.rows_total + grid - 1) / grid;
+        // seg_major: CTAs per segment (one segment per CTA), else one row
+        // range per CTA over every segment
+        a.seg_major = (table && p.seg_major) ? 1 : 0;
+        if (a.seg_major && p.y_sum)
+            return cudaErrorInvalidValue;  // the route-weighted sum is a separate pass
+        const int nseg_cta = (table && !a.seg_major) ? p.n_seg : 1;  // segments each CTA walks
+        int64_t splits = a.seg_major ? std::max<int64_t>(1, di.sm_count / p.n_seg)
+                                     : std::min<int64_t>(di.sm_count, std::max<int64_t>(1, a.rows_total / 2));
+        if (a.seg_major)
+            splits = std::min<int64_t>(splits, std::max<int64_t>(1, a.rows_total / 2));
+        int64_t rows_per_cta = (a.rows_total + splits - 1) / splits;
         // more CTAs (in waves) when one CTA's partial sums would not fit
-        const int64_t per_row = (int64_t)wpg * vp * (table ? p.n_seg : 1) * (int64_t)sizeof(float) / rpt + 1;
+        const int64_t per_row = (int64_t)wpg * vp * nseg_cta * (int64_t)sizeof(float) / rpt + 1;
         while (rows_per_cta * per_row > 48 * 1024 && rows_per_cta > (int64_t)unit_rows * a.sub) {
-            grid += di.sm_count;
-            rows_per_cta = (a.rows_total + grid - 1) / grid;
+            splits += a.seg_major ? splits : di.sm_count;
+            rows_per_cta = (a.rows_total + splits - 1) / splits;
         }
+        const int64_t grid = a.seg_major ? splits * p.n_seg : splits;
+        a.cps = (int)splits;
         // a stage never holds more rows than the CTA owns
         while (a.sub > 1 && (int64_t)unit_rows * a.sub / 2 >= rows_per_cta)
             a.sub = (a.sub + 1) / 2;
         a.rps = unit_rows * a.sub;
         a.stage_bytes = (uint32_t)(a.rps * (int64_t)a.rstride);
 
-        a.rows_q = (int)(a.rows_total / grid);
-        a.rows_r = (int)(a.rows_total % grid);
-        const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? p.n_seg : 2);
+        a.rows_q = (int)(a.rows_total / splits);
+        a.rows_r = (int)(a.rows_total % splits);
+        const int64_t stages_per_cta = ((rows_per_cta + a.rps - 1) / a.rps) * (table ? nseg_cta : 2);
         a.max_stages = (int)stages_per_cta;
         const bool coop = p.act == ACT_BF16 && (sw == 4 || sw == 8) && mc <= 2;
         if (coop && (int64_t)mc * nbc * 16 > (int64_t)kCoopGroupsPerThread * a.tc)
             return cudaErrorInvalidConfiguration;  // not reached: tc >= 4 * nbc and groups >= 2 for m = 2
         const size_t x_bytes = coop ? align16((size_t)coop_x_bytes(mc, nbc)) : align16((size_t)mc * nbc * xbpb);
         // a single activation chunk, read once: stage it in the last ring slot
-        a.x_in_ring = (a.x_bulk && (p.x_seg_stride == 0 || p.n_seg == 1) && x_bytes <= a.stage_bytes) ? 1 : 0;
+        a.x_in_ring = (a.x_bulk && (p.x_seg_stride == 0 || p.n_seg == 1 || a.seg_major) && x_bytes <= a.stage_bytes) ? 1 : 0;
         const size_t red_bytes = sizeof(float) * (size_t)stages_per_cta * a.sub * a.groups * wpg * vp;
         size_t smem = 0;
         int nst = 8;

@@ -215,4 +215,34 @@ cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void*
                       static_cast<uint8_t*>(h_q8), h_bf16);
 }
 
+// ---- route-weighted sum of per-expert outputs ----------------------------------
+// y_sum[n] = sum_e route_w[e] * y_exp[e][n] (moe_v41/init.rs,
+// `moe_v41_accumulate`), one fp32 fmaf per expert in expert order from 0:
+// the same chain as the sum fused into the expert GEMV, so both give the
+// same bits.
+__global__ void __launch_bounds__(256) expert_sum_kernel(const float* __restrict__ y_exp,
+                                                         const float* __restrict__ route_w, int E, int64_t N,
+                                                         float* __restrict__ y_sum)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += (int64_t)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int e = 0; e < E; ++e)
+            acc = fmaf(route_w[e], y_exp[(int64_t)e * N + n], acc);
+        y_sum[n] = acc;
+    }
+}
+
+cudaError_t launch_expert_sum(const float* y_exp, const float* route_w, int64_t E, int64_t N, float* y_sum,
+                              cudaStream_t s)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((N + 255) / 256, (int64_t)di.sm_count * 4));
+    return launch_pdl(expert_sum_kernel, dim3((unsigned)grid), dim3(256), 0, s, y_exp, route_w, (int)E, N, y_sum);
+}
+
 }  // namespace q2k

@@ -49,7 +49,7 @@ def test_size_helpers(L):
     assert L.q2k_row_bytes(300) == 0 and L.q2k_row_bytes(0) == 0
     assert L.q8_1_row_bytes(4096) == 128 * 36
     assert L.q8_1_row_bytes(33) == 0
-    assert L.q2k_moe_m1_workspace_bytes(8, 4096, 2048) == 4608 + 2 * 8 * 2048 * 4 + 8 * 2304
+    assert L.q2k_moe_m1_workspace_bytes(8, 4096, 2048) == 4608 + 2 * 8 * 2048 * 4 + 8 * 2304 + 8 * 4096 * 4
 
 
 def test_status_strings(L):

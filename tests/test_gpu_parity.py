@@ -302,6 +302,31 @@ def test_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
     assert torch.equal(ys2, ysum)
 
 
+@pytest.mark.parametrize("n_mat,N,K,fused", [(160, 64, 256, False), (3, 4096, 2048, True), (24, 300, 1024, True)])
+def test_experts_one_matrix_per_cta_equals_fused_sum(lib, n_mat, N, K, fused):
+    """Per-matrix inputs with y given take one matrix per group of CTAs (more
+    matrices than SMs: several waves) and a separate weighted sum; without y
+    the sum is fused into the GEMV.  Same bits where both apply (the fused
+    path keeps every matrix's partial sums of its rows in shared memory, so
+    it does not take 160 matrices)."""
+    mats = [dev(synth.q2k_matrix(4, f"exm.{n_mat}.{e}", N, K)) for e in range(n_mat)]
+    x = synth.bf16_normal(4, f"exm.x{n_mat}", (n_mat, K))
+    xq = lib.q8_1_quantize_rows(bf16_dev(x))
+    w = np.random.default_rng(n_mat).random(n_mat).astype(np.float32)
+    wt = dev(w)
+    tbl = lib.pointer_table(mats)
+    ysum = torch.empty(N, dtype=torch.float32, device="cuda")
+    y, _ = lib.q2k_mmvq_experts(tbl, N, K, xq, x_per_matrix=True, route_w=wt, y_sum=ysum)
+    for e in sorted({0, n_mat // 2, n_mat - 1}):
+        assert torch.equal(y[e:e + 1], lib.q2k_mmvq_q8_1(mats[e], xq[e:e + 1], K)), e
+    if fused:
+        ys2 = torch.empty(N, dtype=torch.float32, device="cuda")
+        lib.q2k_mmvq_experts(tbl, N, K, xq, x_per_matrix=True, route_w=wt, y_sum=ys2, want_y=False)
+        assert torch.equal(ys2, ysum)
+    ref = (w.astype(np.float64)[:, None] * y.cpu().numpy().astype(np.float64)).sum(0)
+    assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
+
+
 def test_swiglu_q8_1_against_oracle(lib):
     E, N = 3, 2048
     g = np.random.default_rng(3).standard_normal((2 * E, N)).astype(np.float32) * 2
