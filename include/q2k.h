@@ -134,9 +134,9 @@ int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t
  *                equals q2k_mmvq_q8_1(W_table[e], xq row) bit for bit
  *   route_w      fp32 [n_mat], required with y_sum
  *   y_sum        fp32 [N], nullable: y_sum[n] = sum_e route_w[e]*y[e,n],
- *                added in e order (deterministic).  With per-matrix
- *                inputs and y given, each matrix gets CTAs of its own and
- *                the sum is a second launch over y; the bits are the same.
+ *                added in e order (deterministic).  With y given, each
+ *                matrix gets CTAs of its own and the sum is a second
+ *                launch over y; the bits are the same.
  *                Without y the sum is fused: each CTA keeps the partial
  *                sums of all n_mat matrices for its rows in shared memory,
  *                and a problem whose partials do not fit fails with a CUDA

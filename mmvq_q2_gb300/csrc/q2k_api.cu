@@ -280,14 +280,15 @@ int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64
     p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
     p.x_seg_stride = x_per_matrix ? (int64_t)q8_1_row_bytes(K) : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (x_per_matrix && y && y_sum) {
-        // one matrix per CTA (its input row staged once), then the
-        // route-weighted sum over the outputs y in a second pass
+    if (y) {
+        // each matrix gets CTAs of its own (full reduction units, its input
+        // row staged once); the route-weighted sum, if asked for, is a
+        // second pass over y
         p.seg_major = 1;
         p.y_sum = nullptr;
         cudaError_t e = launch_mv(p, s);
-        if (e != cudaSuccess)
-            return fail_cuda(e);
+        if (e != cudaSuccess || !y_sum)
+            return e != cudaSuccess ? fail_cuda(e) : finish(e);
         return finish(launch_expert_sum(y, route_w, n_mat, N, y_sum, s));
     }
     return finish(launch_mv(p, s));
@@ -350,6 +351,7 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     p.W_table = ptrs;
     p.N[0] = inter;
     p.y_exp = gate_up;
+    p.seg_major = 1;  // each gate/up matrix gets CTAs of its own
     p.x = xq;
     p.x_tok_stride = (int64_t)q8_1_row_bytes(dim);
     p.x_seg_stride = 0;
