@@ -140,6 +140,32 @@ def test_gemv_bf16_small(lib, N, K, m):
     assert rel_err_rows(y, ref) <= TOL_BF16
 
 
+# one token over long rows takes whole half blocks per thread (8-word
+# slices): ragged row counts, K not a power of two, rows that are not 16-byte
+# aligned (K = 8448: 2772-byte rows, the 4-byte copy path) and a K split into
+# two chunks that add into y (40960)
+LONG_M1 = [(37, 8192), (100, 8448), (257, 12288), (19, 40960)]
+
+
+@pytest.mark.parametrize("N,K", LONG_M1)
+def test_gemv_bf16_long_rows_one_token(lib, N, K):
+    W = synth.q2k_matrix(6, f"long.{N}.{K}", N, K)
+    x = synth.bf16_normal(6, f"long.x.{K}", (1, K))
+    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+
+
+@pytest.mark.parametrize("N,K", LONG_M1)
+def test_mmvq_q8_1_long_rows_one_token(lib, N, K):
+    W = synth.q2k_matrix(6, f"long.{N}.{K}", N, K)
+    x = synth.bf16_normal(6, f"long.x.{K}", (1, K))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q2k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, 1, K))) <= 1e-4
+    if N >= 32:  # the q8_1 gate against the bf16 values (see the small shapes)
+        assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
+
+
 def test_gemv_bf16_unaligned_weights_take_the_copy_path(lib):
     N, K = 21, 4096
     W = synth.q2k_matrix(5, "unal", N, K)
@@ -258,7 +284,7 @@ def test_pair_ragged_sizes(lib):
     assert torch.equal(yb, lib.q2k_mmvq_q8_1(dev(Wb), xq, K))
 
 
-@pytest.mark.parametrize("m,K", [(6, 8448), (8, 16384)])
+@pytest.mark.parametrize("m,K", [(1, 8448), (1, 16384), (6, 8448), (8, 16384)])
 def test_pair_several_tokens_long_k(lib, m, K):
     # several tokens and several K chunks (the tensor-core path): each output
     # still equals the single call bit for bit, and matches the oracle
@@ -302,7 +328,8 @@ def test_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
     assert torch.equal(ys2, ysum)
 
 
-@pytest.mark.parametrize("n_mat,N,K,fused", [(160, 64, 256, False), (3, 4096, 2048, True), (24, 300, 1024, True)])
+@pytest.mark.parametrize("n_mat,N,K,fused", [(160, 64, 256, False), (3, 4096, 2048, True), (24, 300, 1024, True),
+                                             (4, 200, 8192, True)])
 def test_experts_one_matrix_per_cta_equals_fused_sum(lib, n_mat, N, K, fused):
     """Per-matrix inputs with y given take one matrix per group of CTAs (more
     matrices than SMs: several waves) and a separate weighted sum; without y
