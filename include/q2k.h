@@ -106,7 +106,9 @@ int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx
  * The activations enter the integer dot products as 16-bit fixed point
  * with one power-of-two exponent per 16 values (exact unless a group spans
  * more than 2^7 in magnitude; then the smallest lose bits below 2^-15 of
- * the group maximum); groups below 2^-100 in magnitude count as zero. */
+ * the group maximum).  One token over rows of K >= 8192 uses one exponent
+ * per 32 values and a 2^14 range (exact within 2^6 of the group maximum,
+ * bits below 2^-14 of it lost).  Groups below 2^-100 count as zero. */
 int q2k_gemv_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx,
                   float* y, int64_t ldy, q2k_stream_t stream);
 
@@ -163,7 +165,10 @@ size_t q2k_moe_m1_workspace_bytes(int64_t E, int64_t dim, int64_t inter);
 
 /* The routed-expert step for one token as one call (moe_v41/init.rs): q8_1
  * of x, the 2E gate+up batch, SwiGLU + q8_1 of h, the E down batch, the
- * route-weighted sum.  Five launches on `stream`.
+ * route-weighted sum.  Three launches on `stream`: the q8_1 of x (when x is
+ * 16-byte aligned; a separate launch otherwise) runs inside the gate/up
+ * batch and SwiGLU + q8_1 of h inside the down batch, with the same bits as
+ * the separate steps.
  *   ptrs      device array of 3E device pointers: gate_0..gate_{E-1}
  *             ([inter, dim] each), up_0..up_{E-1} ([inter, dim]),
  *             down_0..down_{E-1} ([dim, inter]) (moe_v41/init.rs, `ptrs_dev`)

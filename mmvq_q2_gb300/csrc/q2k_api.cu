@@ -340,8 +340,13 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     float* gate_up = reinterpret_cast<float*>(ws + round256(q8_1_row_bytes(dim)));
     void* h_q8 = ws + round256(q8_1_row_bytes(dim)) + round256((size_t)2 * E * inter * sizeof(float));
     float* down_out = reinterpret_cast<float*>(static_cast<uint8_t*>(h_q8) + round256((size_t)E * q8_1_row_bytes(inter)));
-    cudaError_t e = launch_q8_1_quantize(x_bf16, 1, dim, dim, xq, s);
-    if (e != cudaSuccess)
+    // A 16-byte aligned x is quantised inside the gate/up GEMV (each CTA
+    // encodes it; the first also stores it in the workspace), and SwiGLU +
+    // q8_1 of h run inside the down GEMV the same way: three launches, the
+    // same bits as the five separate steps.
+    const bool fuse_x = aligned(x_bf16, 16);
+    cudaError_t e = cudaSuccess;
+    if (!fuse_x && (e = launch_q8_1_quantize(x_bf16, 1, dim, dim, xq, s)) != cudaSuccess)
         return fail_cuda(e);
     MvProblem p{};
     p.act = ACT_Q8;
@@ -352,12 +357,14 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     p.N[0] = inter;
     p.y_exp = gate_up;
     p.seg_major = 1;  // each gate/up matrix gets CTAs of its own
-    p.x = xq;
+    p.x = fuse_x ? static_cast<const void*>(x_bf16) : xq;
     p.x_tok_stride = (int64_t)q8_1_row_bytes(dim);
     p.x_seg_stride = 0;
+    if (fuse_x) {
+        p.x_prep = 1;
+        p.x_out = xq;
+    }
     if ((e = launch_mv(p, s)) != cudaSuccess)
-        return fail_cuda(e);
-    if ((e = launch_swiglu_q8_1(gate_up, E, inter, h_q8, nullptr, s)) != cudaSuccess)
         return fail_cuda(e);
     MvProblem d{};
     d.act = ACT_Q8;
@@ -371,6 +378,10 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     d.x = h_q8;
     d.x_tok_stride = (int64_t)q8_1_row_bytes(inter);
     d.x_seg_stride = (int64_t)q8_1_row_bytes(inter);
+    d.x_prep = 2;  // h = SwiGLU(gate, up) -> q8_1 per CTA, also stored in h_q8
+    d.gu = gate_up;
+    d.gu_E = E;
+    d.x_out = h_q8;
     if ((e = launch_mv(d, s)) != cudaSuccess)
         return fail_cuda(e);
     return finish(launch_expert_sum(down_out, route_w, E, dim, y, s));

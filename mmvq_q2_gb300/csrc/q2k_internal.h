@@ -39,6 +39,14 @@ struct MvProblem {
     int64_t x_seg_stride;    // bytes between segments' inputs (0 = shared)
     int seg_major;           // table, per-segment inputs, no y_sum: each CTA
                              // works on one segment (its input staged once)
+    // q8_1 activations prepared inside the GEMV (m = 1, q8_1, bulk-copyable
+    // sources): 1 = x is a bf16 row, quantised per CTA; 2 = segment e's input
+    // is SwiGLU(gu[e], gu[gu_E + e]) of fp32 rows of length K, quantised per
+    // CTA.  x_out, when set, receives the q8_1 rows (row e at e * x_seg_stride).
+    int x_prep;
+    const float* gu;
+    int64_t gu_E;
+    void* x_out;
 };
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);

@@ -31,6 +31,7 @@
 //    fuses the experts' route-weighted sum.
 #include "q2k_common.cuh"
 #include "q2k_internal.h"
+#include "q2k_q8.cuh"
 
 #include <algorithm>
 
@@ -56,6 +57,8 @@ struct MvArgs {
     int seg_major;  // table only: CTA c works on segment c / cps alone, rows
                     // split cps ways (per-segment activations staged once)
     int cps;        // CTAs per segment (seg_major)
+    int x_prep;     // 0: activations as given; 1: bf16 x quantised to q8_1 here;
+                    // 2: q8_1 of SwiGLU(gu[e], gu[gu_E + e]) made here
     int N[2];
     int x_bulk;     // 1: the first segment's activations arrive by bulk copy
     int x_in_ring;  // 1: they arrive in the last ring slot, which the
@@ -73,6 +76,10 @@ struct MvArgs {
     int64_t x_seg_stride;
     const uint8_t* W[2];
     const void* const* W_table;
+    const float* gu;  // x_prep 2: fp32 gate rows [gu_E][gu_ld], then up rows
+    uint8_t* x_out;   // x_prep: the prepared q8_1 rows are also stored here
+    int64_t gu_ld;    // floats per gu row
+    int gu_E;
     // decomposition
     int s_real;         // slices per row
     int s_pad;          // lanes per row group
@@ -552,6 +559,38 @@ __device__ __forceinline__ void slice_dot(const Slice<M, ACT, SW>& sl, const uin
     }
 }
 
+// q8_1 activations made inside the kernel from the source rows staged at
+// xsm + raw_off (one token): x_prep 1 quantises a bf16 row, x_prep 2 takes
+// SwiGLU of an fp32 gate row and an fp32 up row first.  The same encoder and
+// SwiGLU as the standalone kernels, so the bits are the same.  All threads.
+template <typename Args>
+__device__ __forceinline__ void prep_x_q8(const Args& a, uint8_t* xsm, int raw_off, int warp, int lane, int nwarps)
+{
+    const int nlanes = a.nbc * 8 * 8;  // q8_1 blocks of the chunk x 8 lanes
+    const uint8_t* raw = xsm + raw_off;
+    for (int wbase = warp * 32; wbase < nlanes; wbase += nwarps * 32) {  // warp-uniform
+        const int u = wbase + lane;
+        const bool live = u < nlanes;
+        const int uu = live ? u : wbase;
+        const int lane8 = uu & 7, blk = uu >> 3;
+        const int k0 = blk * kQ8Values + 4 * lane8;
+        float v[4];
+        if (a.x_prep == 1) {
+            const uint16_t* xb = reinterpret_cast<const uint16_t*>(raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = live ? bf16_bits_f(xb[k0 + i]) : 0.f;
+        } else {
+            const float* g = reinterpret_cast<const float*>(raw);
+            const float* up = g + a.nbc * 256;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = live ? __bfloat162float(swiglu_bf16(g[k0 + i], up[k0 + i])) : 0.f;
+        }
+        q8_1_encode_group(v, xsm + blk * kQ8Bytes, lane8, live);
+    }
+}
+
 __device__ __forceinline__ void flag_error(volatile int* abort_flag)
 {
     atomicOr(&g_mv_error, Q2K_ERR_BIT_WAIT_TIMEOUT);
@@ -643,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
     };
     const bool x_first_bulk = a.x_bulk && nstages > 0;
     const int x_rowb = a.nbc * x_bytes_per_block<ACT>();
+    const int x_rowb16 = (x_rowb + 15) & ~15;  // prepared activations: the source rows follow
 
     const uint32_t chunk = (uint32_t)a.nbc * kBlockBytes;
     // Bulk copy of stage st into a ring slot (lane 0 only; the source rows
@@ -690,12 +730,28 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         if (x_first_bulk) {
             // the activations first, ahead of the weight prefetch
             const int e0 = stage_at(a, lo, hi, 0, seg).e;
-            const uint8_t* xs0 = a.x + (int64_t)e0 * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
             const uint64_t pol = l2_policy_evict_last();  // every CTA reads them
-            mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
-            for (int t = 0; t < M; ++t)
-                bulk_copy_g2s_hint(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
-                                   smem_u32(xbar), pol);
+            if (ACT == ACT_Q8 && a.x_prep == 1) {
+                // the bf16 row, quantised to q8_1 below
+                const uint32_t raw = (uint32_t)a.nbc * 512u;
+                mbar_arrive_expect_tx(smem_u32(xbar), raw);
+                bulk_copy_g2s_hint(smem_u32(xsm + x_rowb16), a.x + (int64_t)a.kb0 * 512, raw, smem_u32(xbar), pol);
+            } else if (ACT == ACT_Q8 && a.x_prep == 2) {
+                // the fp32 gate and up rows of segment e0, SwiGLU + q8_1 below
+                const uint32_t raw = (uint32_t)a.nbc * 1024u;
+                mbar_arrive_expect_tx(smem_u32(xbar), 2 * raw);
+                const float* g0 = a.gu + (int64_t)e0 * a.gu_ld + (int64_t)a.kb0 * 256;
+                const float* u0 = a.gu + (int64_t)(a.gu_E + e0) * a.gu_ld + (int64_t)a.kb0 * 256;
+                bulk_copy_g2s_hint(smem_u32(xsm + x_rowb16), g0, raw, smem_u32(xbar), pol);
+                bulk_copy_g2s_hint(smem_u32(xsm + x_rowb16 + raw), u0, raw, smem_u32(xbar), pol);
+            } else {
+                const uint8_t* xs0 =
+                    a.x + (int64_t)e0 * a.x_seg_stride + (int64_t)a.kb0 * x_bytes_per_block<ACT>();
+                mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * x_rowb));
+                for (int t = 0; t < M; ++t)
+                    bulk_copy_g2s_hint(smem_u32(xsm + t * x_rowb), xs0 + t * a.x_tok_stride, (uint32_t)x_rowb,
+                                       smem_u32(xbar), pol);
+            }
         }
     }
     // The first stage goes out right behind the activations; the other
@@ -822,6 +878,19 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
         aborted = !warp_wait(smem_u32(xbar), 0, abort_flag, lane);
         if (warp > 0 && warp < pre)
             produce(warp);  // the rest of the prologue stages, now the activations are in
+        if constexpr (ACT == ACT_Q8 && M == 1) {
+            if (a.x_prep) {  // uniform across the CTA
+                prep_x_q8(a, xsm, x_rowb16, warp, lane, nwarps);
+                __syncthreads();
+                // the prepared rows also go out (the first CTA of each
+                // segment; a shared row is written once)
+                if (a.x_out && cta == 0 && (a.x_prep == 2 || seg == 0)) {
+                    uint8_t* dst = a.x_out + (int64_t)seg * a.x_seg_stride + (int64_t)a.kb0 * 8 * kQ8Bytes;
+                    for (int o = tid * 4; o < x_rowb; o += blockDim.x * 4)
+                        *reinterpret_cast<uint32_t*>(dst + o) = *reinterpret_cast<const uint32_t*>(xsm + o);
+                }
+            }
+        }
         if constexpr (coop_x<M, ACT, SW>())
             convert_x_bf16<M, SW>(xsm, a.nbc);  // every thread (the condition is uniform)
         load_slice<M, ACT, SW>(sl, xsm, a.nbc, b, n, wi0, active);
@@ -1109,6 +1178,20 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
             a.x_align = (bits & 15u) == 0 ? 16 : ((bits & 3u) == 0 ? 4 : 2);
             a.x_bulk = a.x_align == 16 ? 1 : 0;
         }
+        a.x_prep = p.x_prep;
+        a.gu = p.gu;
+        a.gu_E = (int)p.gu_E;
+        a.gu_ld = p.K;
+        a.x_out = static_cast<uint8_t*>(p.x_out);
+        if (p.x_prep) {
+            // prepared activations: one token, q8_1, sources a bulk copy can read
+            const uintptr_t src = p.x_prep == 1 ? reinterpret_cast<uintptr_t>(p.x) : reinterpret_cast<uintptr_t>(p.gu);
+            if (p.act != ACT_Q8 || mc != 1 || (p.x_prep == 2 && (!p.gu || !table || p.gu_E < p.n_seg)) ||
+                (src & 15u) != 0)
+                return cudaErrorInvalidValue;
+            a.x_align = 16;
+            a.x_bulk = 1;
+        }
         for (int e = 0; e < 2; ++e) {
             a.y[e] = p.y[e];
             a.ldy[e] = p.ldy[e];
@@ -1169,7 +1252,9 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         const bool coop = p.act == ACT_BF16 && (sw == 4 || sw == 8) && mc <= 2;
         if (coop && (int64_t)mc * nbc * 16 > (int64_t)kCoopGroupsPerThread * a.tc)
             return cudaErrorInvalidConfiguration;  // not reached: tc >= 4 * nbc and groups >= 2 for m = 2
-        const size_t x_bytes = coop ? align16((size_t)coop_x_bytes(mc, nbc)) : align16((size_t)mc * nbc * xbpb);
+        size_t x_bytes = coop ? align16((size_t)coop_x_bytes(mc, nbc)) : align16((size_t)mc * nbc * xbpb);
+        if (p.x_prep)  // the source rows follow the q8_1 rows
+            x_bytes += (size_t)nbc * (p.x_prep == 1 ? 512 : 2048);
         // a single activation chunk, read once: stage it in the last ring slot
         a.x_in_ring = (a.x_bulk && (p.x_seg_stride == 0 || p.n_seg == 1 || a.seg_major) && x_bytes <= a.stage_bytes) ? 1 : 0;
         const size_t red_bytes = sizeof(float) * (size_t)stages_per_cta * a.sub * a.groups * wpg * vp;
