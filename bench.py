@@ -414,6 +414,13 @@ def sweep(q, L, l2, hbm, rank):
             check(L.q2k_mmvq_pair(P(Was[i % R]), 1024, P(ya), P(Wbs[i % R]), 512, P(yb), K, P(xq), m, cur()), "pair")
         el, n = graph_time(pair, 2000, 100)
         rec(f"pair (q8_1 + wq_a/wkv) m={m}", el / n, Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
+        # the same as one call from bf16 (the q8_1 encoding inside the pair launch for m = 1)
+        def pair_bf16(i):
+            check(L.q2k_mmvq_pair_bf16(P(Was[i % R]), 1024, P(ya), P(Wbs[i % R]), 512, P(yb), K, P(xd), m, P(xq),
+                                       cur()), "pair_bf16")
+        el, n = graph_time(pair_bf16, 2000, 100)
+        rec(f"pair from bf16 (q8_1 inside the call) m={m}", el / n,
+            Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
     del Was, Wbs
 
     # cfg3: routed experts for one token (256 experts resident, selection varies per call)

@@ -125,6 +125,19 @@ int q2k_mmvq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m
 int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb,
                   int64_t K, const void* xq, int64_t m, q2k_stream_t stream);
 
+/* The pair over bf16 activations: the q8_1 quantisation of x
+ * (q8_1_quantize_rows) and q2k_mmvq_pair as one call (attn_v41/decode.rs,
+ * `q_kv_projections`: one q8_1 quantisation feeds one launch for both).
+ *   x_bf16  [m, K] bf16 rows back to back
+ *   xq_out  m q8_1 rows; receives q8_1_quantize_rows(x) in every case
+ *   Wa, Na, ya, Wb, Nb, yb, K, m  as for q2k_mmvq_pair
+ * For m = 1 and a 16-byte aligned x the encoding runs inside the pair
+ * launch (each CTA encodes the row; one launch).  Otherwise it is a launch
+ * of its own, then the pair.  Either way xq_out, ya and yb equal the two
+ * separate calls bit for bit. */
+int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb,
+                       int64_t K, const uint16_t* x_bf16, int64_t m, void* xq_out, q2k_stream_t stream);
+
 /* Batched single-token MMVQ over n_mat Q2_K matrices of one shape, with an
  * optional fused route-weighted sum (moe_v41/init.rs,
  * `kquant_mmvq_q2_k_experts_w8`, `moe_v41_accumulate`).

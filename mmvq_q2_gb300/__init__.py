@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libq2k.so")
 # Every entry point include/q2k.h declares.
 EXPORTS = (
     "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16",
-    "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_experts", "swiglu_q8_1_rows",
+    "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_experts", "swiglu_q8_1_rows",
     "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
     "q2k_last_cuda_error", "q2k_device_error",
 )
@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "q2k_gemv_bf16": (I32, [P, I64, I64, P, I64, I64, P, I64, P]),
             "q2k_mmvq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P]),
             "q2k_mmvq_pair": (I32, [P, I64, P, P, I64, P, I64, P, I64, P]),
+            "q2k_mmvq_pair_bf16": (I32, [P, I64, P, P, I64, P, I64, P, I64, P, P]),
             "q2k_mmvq_experts": (I32, [P, I64, I64, I64, P, I32, P, P, P, P]),
             "swiglu_q8_1_rows": (I32, [P, I64, I64, P, P, P]),
             "q2k_moe_m1_workspace_bytes": (SZ, [I64, I64, I64]),
@@ -174,6 +175,24 @@ def q2k_mmvq_pair(Wa, Wb, xq, K, ya=None, yb=None, stream=None):
         yb = torch.empty((m, Nb), dtype=torch.float32, device=xq.device)
     _call("q2k_mmvq_pair", _ptr(Wa), Na, _ptr(ya), _ptr(Wb), Nb, _ptr(yb), K, _ptr(xq), m, _stream(stream))
     return ya, yb
+
+
+def q2k_mmvq_pair_bf16(Wa, Wb, x, K, ya=None, yb=None, xq=None, stream=None):
+    """The pair over bf16 rows ``x [m, K]``, with the q8_1 encoding of x in
+    the same call (inside the one launch for m = 1) -> (ya, yb, xq)."""
+    _need_cuda(Wa, Wb, x, ya, yb, xq)
+    m = x.shape[0]
+    Na = Wa.numel() // q2k_row_bytes(K)
+    Nb = Wb.numel() // q2k_row_bytes(K)
+    if ya is None:
+        ya = torch.empty((m, Na), dtype=torch.float32, device=x.device)
+    if yb is None:
+        yb = torch.empty((m, Nb), dtype=torch.float32, device=x.device)
+    if xq is None:
+        xq = torch.empty((m, q8_1_row_bytes(K)), dtype=torch.uint8, device=x.device)
+    _call("q2k_mmvq_pair_bf16", _ptr(Wa), Na, _ptr(ya), _ptr(Wb), Nb, _ptr(yb), K, _ptr(x), m, _ptr(xq),
+          _stream(stream))
+    return ya, yb, xq
 
 
 def pointer_table(tensors, device=None):

@@ -252,6 +252,48 @@ int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t
     return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb, int64_t K,
+                       const uint16_t* x_bf16, int64_t m, void* xq_out, q2k_stream_t stream)
+{
+    if (!Wa || !Wb || !ya || !yb || !x_bf16 || !xq_out)
+        return Q2K_ERR_NULL_ARG;
+    if (Na <= 0 || Nb <= 0 || K <= 0 || K % kBlockWeights || K > kMaxK || m < 1 || m > 8)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(Wa, 4) || !aligned(Wb, 4) || !aligned(ya, 4) || !aligned(yb, 4) || !aligned(x_bf16, 2) ||
+        !aligned(xq_out, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = (int)m;
+    p.K = K;
+    p.n_seg = 2;
+    p.W[0] = Wa;
+    p.W[1] = Wb;
+    p.N[0] = Na;
+    p.N[1] = Nb;
+    p.y[0] = ya;
+    p.y[1] = yb;
+    p.ldy[0] = Na;
+    p.ldy[1] = Nb;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    if (m == 1 && aligned(x_bf16, 16)) {
+        // one launch: every CTA encodes the row, the first also stores it
+        p.x = x_bf16;
+        p.x_prep = 1;
+        p.x_out = xq_out;
+        return finish(launch_mv(p, s));
+    }
+    cudaError_t e = launch_q8_1_quantize(x_bf16, m, K, K, xq_out, s);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    p.x = xq_out;
+    return finish(launch_mv(p, s));
+}
+
 int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K, const void* xq,
                      int x_per_matrix, float* y, const float* route_w, float* y_sum, q2k_stream_t stream)
 {

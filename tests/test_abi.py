@@ -82,6 +82,11 @@ def test_mmvq_pair_experts_validation(L):
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 0, None) == 2
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, None, 4, FAKE, 512, FAKE, 1, None) == 1
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, -1, FAKE, 512, FAKE, 1, None) == 2
+    # the pair over bf16 rows: the q8_1 destination is required; x is 2-byte aligned
+    assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 1, None, None) == 1
+    assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 9, FAKE, None) == 2
+    assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 500, FAKE, 1, FAKE, None) == 2
+    assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, P(0x10001), 1, FAKE, None) == 3
     # experts: y_sum needs route weights; x_per_matrix is 0 or 1
     assert L.q2k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, None, None, FAKE, None) == 1
     assert L.q2k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, None, None, None, None) == 1

@@ -273,6 +273,24 @@ def test_pair_cfg2_equals_two_singles_bitwise(lib, m):
     assert rel_err_rows(yb.cpu().numpy(), oracle.matvec(Wb, 512, K, x_f64(x))) <= TOL_Q8
 
 
+@pytest.mark.parametrize("m,K,off", [(1, 4096, 0), (1, 8448, 0), (1, 4096, 1), (4, 4096, 0)])
+def test_pair_bf16_equals_quantise_then_pair(lib, m, K, off):
+    """The one-call pair over bf16 rows (q8_1 made inside the launch for an
+    aligned single row; a launch of its own otherwise, off = 1 element)."""
+    Wa = synth.q2k_matrix(7, f"pb.a.{K}", 1024, K)
+    Wb = synth.q2k_matrix(7, f"pb.b.{K}", 130, K)
+    x = synth.bf16_normal(7, f"pb.x.{m}.{K}", (m, K))
+    buf = torch.zeros(m * K + 8, dtype=torch.int16, device="cuda")
+    buf[off:off + m * K] = torch.from_numpy(x.view(np.int16).reshape(-1)).cuda()
+    xd = buf[off:off + m * K].view(m, K).view(torch.bfloat16)
+    ya, yb, xq = lib.q2k_mmvq_pair_bf16(dev(Wa), dev(Wb), xd, K)
+    xq2 = lib.q8_1_quantize_rows(xd)
+    ya2, yb2 = lib.q2k_mmvq_pair(dev(Wa), dev(Wb), xq2, K)
+    assert torch.equal(xq, xq2)
+    assert torch.equal(ya, ya2) and torch.equal(yb, yb2)
+    np.testing.assert_array_equal(xq.cpu().numpy(), oracle.q8_1_quantize(x))
+
+
 def test_pair_ragged_sizes(lib):
     K = 768
     Wa = synth.q2k_matrix(1, "pr.a", 37, K)
