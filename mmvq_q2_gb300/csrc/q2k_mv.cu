@@ -6,29 +6,39 @@
 // batches, `moe_v41_accumulate` route-weighted sum).
 //
 // Design (GB300, one CTA of 16 warps per SM):
-//  * Weight rows stream into a ring of ~40 KB shared-memory stages with 1-D
-//    bulk asynchronous copies (cp.async.bulk, the TMA engine) signalled on
-//    mbarriers.  Warp 0 primes the ring; afterwards the last warp to finish
-//    with a slot (a shared-memory counter) refills it, so no warp ever
-//    blocks to produce.  Rows that are not 16-byte aligned are copied with
-//    4-byte loads instead.  Every wait is bounded.
-//  * The activations of the CTA's K chunk are staged once in shared memory;
+//  * Weight rows stream into a ring of shared-memory stages (one or more
+//    reduction units of rows, up to ~86 KB) with 1-D bulk asynchronous
+//    copies (cp.async.bulk, the TMA engine) signalled on mbarriers.  Warp w
+//    primes slot w; afterwards any warp may claim the refill of a slot that
+//    every warp has released (a compare-and-swap on the next stage to
+//    issue), so no warp is dedicated to producing.  Rows that are not
+//    16-byte aligned are copied with 4-byte loads instead.  Every wait is
+//    bounded.
+//  * The activations of the CTA's K chunk are staged once in shared memory
+//    (or made there: q8_1 of a bf16 row, or of SwiGLU of fp32 gate/up rows);
 //    each thread then owns a fixed K-slice of every row (SW words of a
-//    block's qs: 16*SW weights over 4 sub-blocks) and keeps the matching
+//    block's qs: 16*SW weights over 4 sub-blocks; 8 words, a whole half
+//    block, for one token over long rows) and keeps the matching
 //    activations in registers for all rows it visits, so the only per-row
 //    traffic is the weight stream itself.
 //  * Codes are extracted four at a time with one AND per register (the code
 //    of pair j stays at bit 2j of each byte, i.e. scaled by 4^j; the 4^-j is
 //    folded into the activation scale) and multiplied by DP4A (q8_1
 //    activations) or two DP2A (bf16 activations as 16-bit fixed point with
-//    one exponent per group of 16).
+//    one exponent per group of 16, or per 32 for 8-word slices).
 //  * Per sub-block: y += d*sc*xscale*S - dmin*m*sum(x).  S*sc is formed in
-//    int32; the min term is a dot product of the min nibbles with the
-//    group sums (16-bit fixed point, one exponent per slice).
+//    int32 (with 8-word slices the two halves of a bit plane meet in int32
+//    too); the min term is a dot product of the min nibbles with the group
+//    sums (16-bit fixed point, one exponent per slice).
 //  * Partial sums: a transpose-reduce across each warp's lanes deposits one
 //    (row, token) sum per warp in shared memory; after the stage loop the
 //    warps' sums are added in a fixed order (deterministic), which also
-//    fuses the experts' route-weighted sum.
+//    fuses the experts' route-weighted sum when one CTA walks every expert
+//    of its rows.  With per-expert outputs each expert gets CTAs of its own
+//    instead (segment-major), and the weighted sum is a separate pass.
+//  * The kernel is a programmatic dependent launch: it touches no global
+//    memory before griddepcontrol.wait, so its setup overlaps the previous
+//    kernel in the stream.
 #include "q2k_common.cuh"
 #include "q2k_internal.h"
 #include "q2k_q8.cuh"
