@@ -17,11 +17,12 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   and x from pinned host memory, calls the C ABI, and reads y back.
 * cpu_baseline times the CPU oracle (one thread) on a bounded sample.
 * --impl reference times the CPU oracle on the same workload (rank 0 only).
-* --ncu-case [mv|mt|gemm] runs a few untimed calls for a profiler capture
-  and prints no JSON line: mv = the headline kernel (bf16 GEMV) and the q8_1
-  MMVQ at m=1 on the headline shape; mt = the same shape at m=8 (the
-  tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
-  N=K=16384.
+* --ncu-case [mv|mt|gemm|small] runs a few untimed calls for a profiler
+  capture and prints no JSON line: mv = the headline kernel (bf16 GEMV) and
+  the q8_1 MMVQ at m=1 on the headline shape; mt = the same shape at m=8
+  (the tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
+  N=K=16384; small = one call of every other kernel at the configurations'
+  shapes.
 * --all also times every configuration of the sweep and prints one JSON
   object per configuration to stderr (and to gpurun_out/bench_all.jsonl when
   that folder exists).
@@ -527,6 +528,45 @@ def run_reference(args):
     }
 
 
+def _ncu_small_case(q):
+    """One call of every other kernel, at the configurations' shapes: the
+    engram rows + m=16 GEMM (cfg1), the pair at m=1 (cfg2, q8_1 made
+    separately and inside the launch), the MoE step (cfg3, three launches),
+    the standalone SwiGLU, the fused-sum expert batch and the weighted sum,
+    and a dense GEMM below 16 tokens (the mma.sync kernel)."""
+    import torch
+    dev = lambda a: torch.from_numpy(a).cuda()
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    # cfg1: 128 engram rows of a 2^20-row table, then [16, 2048] x wkv^T
+    table = dev(synth.q2k_blocks(0, "cfg1.table", 1 << 20))
+    ids = dev(synth.row_ids(0, "cfg1.ids", 128, 1 << 20))
+    wkv = bf(synth.bf16_normal(0, "cfg1.wkv", (20480, 2048), std=0.02))
+    rows = q.q2k_dequant_rows(table, 256, ids=ids)
+    q.dense_gemm_bf16(rows.view(16, 2048), wkv)
+    q.dense_gemm_bf16(rows.view(16, 2048)[:8], wkv)  # m = 8: the mma.sync kernel
+    # cfg2: the pair at m = 1
+    Wa = dev(synth.q2k_matrix(0, "cfg2.wq_a", 1024, 4096))
+    Wb = dev(synth.q2k_matrix(0, "cfg2.wkv", 512, 4096))
+    x = bf(synth.bf16_normal(0, "cfg2.x1", (1, 4096)))
+    xq = q.q8_1_quantize_rows(x)
+    q.q2k_mmvq_pair(Wa, Wb, xq, 4096)
+    q.q2k_mmvq_pair_bf16(Wa, Wb, x, 4096)
+    # cfg3: 8 experts; the MoE step, then its pieces
+    E, dim, inter = 8, 4096, 2048
+    mats = [dev(synth.q2k_matrix(0, f"cfg3.{k}{e}", *shape)) for k, shape in
+            (("gate", (inter, dim)), ("up", (inter, dim)), ("down", (dim, inter))) for e in range(E)]
+    tbl = q.pointer_table(mats)
+    w = torch.full((E,), 0.125, dtype=torch.float32, device="cuda")
+    xm = bf(synth.bf16_normal(0, "cfg3.x", (dim,)))
+    q.q2k_moe_m1(tbl, E, dim, inter, xm, w)
+    gu, _ = q.q2k_mmvq_experts(q.pointer_table(mats[:2 * E]), inter, dim, q.q8_1_quantize_rows(xm.view(1, dim)))
+    hq, _ = q.swiglu_q8_1_rows(gu)
+    ys = torch.empty(dim, dtype=torch.float32, device="cuda")
+    q.q2k_mmvq_experts(q.pointer_table(mats[2 * E:]), dim, inter, hq, x_per_matrix=True, route_w=w, y_sum=ys,
+                       want_y=False)
+    q.q2k_mmvq_experts(q.pointer_table(mats[2 * E:]), dim, inter, hq, x_per_matrix=True, route_w=w, y_sum=ys)
+
+
 def run_ncu_case(which: str = "mv", calls: int = 3):
     """A small fixed workload for a profiler (the profiler flushes the caches
     between passes; one weight copy).  mv: `calls` eager calls of
@@ -537,6 +577,11 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     from mmvq_q2_gb300 import build as b
     b.build()
     import mmvq_q2_gb300 as q
+    if which == "small":
+        _ncu_small_case(q)
+        torch.cuda.synchronize()
+        print("ncu case done", file=sys.stderr)
+        return
     if which == "gemm":
         W = synth.bf16_normal(0, "sweep.dense.W", (N_HEAD, K_HEAD), std=0.02)
         Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
@@ -566,7 +611,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
-    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm"], default=None)
+    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
