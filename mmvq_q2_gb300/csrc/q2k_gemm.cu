@@ -1,5 +1,7 @@
 // Dense bf16 GEMM y = x W^T, fp32 accumulate and output, for the
 // multi-token rows (engram_v41/apply.rs, `ops::dense_gemm` when tokens > 1).
+// Sixteen tokens or more go to the tcgen05 kernel (q2k_umma.cu); this
+// mma.sync kernel takes fewer, below that kernel's smallest MMA width.
 //
 // Weights are streamed once per token tile: a CTA owns 64 weight rows and a
 // tile of up to 64 tokens, stages W and x tiles through a 4-deep cp.async

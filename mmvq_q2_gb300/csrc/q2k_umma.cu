@@ -12,9 +12,13 @@
 //   warps 2..5  read the accumulator back (tcgen05.ld, one TMEM lane per
 //               W row) and store y, coalesced along N.
 // K is split across CTAs when there are too few tiles to fill the GPU; the
-// splits then add into y with fp32 atomics (y is cleared first).
+// splits then add into y with fp32 atomics (y is cleared first).  When the
+// tiles outnumber the SMs the ring is capped so that two CTAs share an SM
+// (no second wave for the few tiles past one per SM).
 // Every wait is bounded: on a timeout the kernel raises its error word,
-// still frees its tensor memory and returns.
+// still frees its tensor memory and returns.  The kernel is a programmatic
+// dependent launch: barriers and tensor memory are set up before it waits
+// for the previous grid.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -312,6 +316,7 @@ cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_
     a.atomic = splits > 1 ? 1 : 0;
     const size_t smem_cap = std::min<size_t>((size_t)di.smem_optin, 224 * 1024);
     const size_t fixed = 1024 + 64 + 16 * 8;
+    // more tiles than SMs: two CTAs per SM rather than a second wave
     const size_t cap2 = (gx * gy * splits > di.sm_count) ? std::min<size_t>(smem_cap, 112 * 1024) : smem_cap;
     a.nst = (int)std::min<size_t>(8, (cap2 - fixed) / a.stage_bytes);
     if (a.nst < 2)
