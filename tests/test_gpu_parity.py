@@ -194,17 +194,22 @@ def test_gemv_bf16_output_stride_and_guard(lib):
     assert rel_err_rows(b[:, :N], oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
 
 
-def test_gemv_bf16_extreme_activation_ranges(lib):
-    # groups with mixed magnitudes, tiny values and zeros
-    N, K = 16, 1024
-    W = synth.q2k_matrix(7, "ext", N, K)
+@pytest.mark.parametrize("K,one_token", [(1024, False), (8192, True)])
+def test_gemv_bf16_extreme_activation_ranges(lib, K, one_token):
+    # groups with mixed magnitudes, tiny values and zeros; K = 8192 one row
+    # at a time takes the 8-word slices (one exponent per 32 values)
+    N = 16
+    W = synth.q2k_matrix(7, f"ext.{K}", N, K)
     v = np.random.default_rng(7).standard_normal((2, K)).astype(np.float32)
     v[0, ::3] *= 1e-4
     v[0, 5::7] = 0.0
     v[1] *= 1e20
     v[1, :64] = 0.0
     x = synth.f32_to_bf16_bits(v)
-    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    if one_token:
+        y = np.concatenate([lib.q2k_gemv_bf16(dev(W), bf16_dev(x[t:t + 1])).cpu().numpy() for t in range(2)])
+    else:
+        y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
     assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
 
 
