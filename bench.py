@@ -424,6 +424,21 @@ def sweep(q, L, l2, hbm, rank):
             Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
     del Was, Wbs
 
+    # grouped (block-diagonal) wo_a MMVQ, the next row: 8 groups of 1024 rows, 2048 values per group
+    G, Rg, Kg = 8, 1024, 2048
+    Wg = synth.q2k_matrix(0, "grouped.wo_a", G * Rg, Kg)
+    R = copies_for(Wg.nbytes, l2)
+    Wgs = [torch.from_numpy(Wg).cuda() for _ in range(R)]
+    for m in (1, 8):
+        x = synth.bf16_normal(0, f"grouped.x{m}", (m, G * Kg))
+        xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        xq = q.q8_1_quantize_rows(xd)
+        yg = torch.empty((m, G * Rg), dtype=torch.float32, device="cuda")
+        el, n = graph_time(lambda i: check(L.q2k_mmvq_grouped(P(Wgs[i % R]), G, Rg, Kg, P(xq), m, P(yg), cur()),
+                                           "grouped"), 2000, 100)
+        rec(f"grouped wo_a MMVQ {G}x[{Rg},{Kg}] m={m}", el / n, Wg.nbytes + xq.numel() + 4 * m * G * Rg, m)
+    del Wgs
+
     # cfg3: routed experts for one token (256 experts resident, selection varies per call)
     E_all, topk, dim, inter = 256, 8, 4096, 2048
     mats = {}

@@ -138,6 +138,21 @@ int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t
 int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb,
                        int64_t K, const uint16_t* x_bf16, int64_t m, void* xq_out, q2k_stream_t stream);
 
+/* Grouped (block-diagonal) MMVQ, m = 1..8 (attn_v41/decode.rs,
+ * `attend_and_project`: og[t, g*o_rank + r] = o_g . wo_a[g*o_rank + r], the
+ * Q2_K `wo_a_grouped` path for m <= 8).
+ *   W       Q2_K [groups * rows_per_group, K_group]: group g owns rows
+ *           g*rows_per_group .. (g+1)*rows_per_group - 1
+ *   xq      m q8_1 rows of groups * K_group values; group g's input is
+ *           values g*K_group .. (g+1)*K_group - 1 of each row
+ *   y       fp32 [m, groups * rows_per_group]:
+ *           y[t, g*rows_per_group + r] = sum_k W[g*rows_per_group + r, k] *
+ *           x_t[g*K_group + k]
+ * One launch; each group's output equals q2k_mmvq_q8_1 of its row block and
+ * its input slice bit for bit (m = 1). */
+int q2k_mmvq_grouped(const void* W, int64_t groups, int64_t rows_per_group, int64_t K_group,
+                     const void* xq, int64_t m, float* y, q2k_stream_t stream);
+
 /* Batched single-token MMVQ over n_mat Q2_K matrices of one shape, with an
  * optional fused route-weighted sum (moe_v41/init.rs,
  * `kquant_mmvq_q2_k_experts_w8`, `moe_v41_accumulate`).

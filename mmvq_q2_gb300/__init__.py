@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libq2k.so")
 # Every entry point include/q2k.h declares.
 EXPORTS = (
     "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16",
-    "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_experts", "swiglu_q8_1_rows",
+    "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_grouped", "q2k_mmvq_experts",
+    "swiglu_q8_1_rows",
     "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
     "q2k_last_cuda_error", "q2k_device_error",
 )
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "q2k_mmvq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P]),
             "q2k_mmvq_pair": (I32, [P, I64, P, P, I64, P, I64, P, I64, P]),
             "q2k_mmvq_pair_bf16": (I32, [P, I64, P, P, I64, P, I64, P, I64, P, P]),
+            "q2k_mmvq_grouped": (I32, [P, I64, I64, I64, P, I64, P, P]),
             "q2k_mmvq_experts": (I32, [P, I64, I64, I64, P, I32, P, P, P, P]),
             "swiglu_q8_1_rows": (I32, [P, I64, I64, P, P, P]),
             "q2k_moe_m1_workspace_bytes": (SZ, [I64, I64, I64]),
@@ -193,6 +195,17 @@ def q2k_mmvq_pair_bf16(Wa, Wb, x, K, ya=None, yb=None, xq=None, stream=None):
     _call("q2k_mmvq_pair_bf16", _ptr(Wa), Na, _ptr(ya), _ptr(Wb), Nb, _ptr(yb), K, _ptr(x), m, _ptr(xq),
           _stream(stream))
     return ya, yb, xq
+
+
+def q2k_mmvq_grouped(W, groups, rows_per_group, K_group, xq, y=None, stream=None):
+    """Block-diagonal MMVQ: group g's rows of ``W`` against group g's slice of
+    each q8_1 row of ``xq`` -> fp32 ``[m, groups * rows_per_group]``."""
+    _need_cuda(W, xq, y)
+    m = xq.shape[0]
+    if y is None:
+        y = torch.empty((m, groups * rows_per_group), dtype=torch.float32, device=xq.device)
+    _call("q2k_mmvq_grouped", _ptr(W), groups, rows_per_group, K_group, _ptr(xq), m, _ptr(y), _stream(stream))
+    return y
 
 
 def pointer_table(tensors, device=None):

@@ -294,6 +294,36 @@ int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, in
     return finish(launch_mv(p, s));
 }
 
+int q2k_mmvq_grouped(const void* W, int64_t groups, int64_t rows_per_group, int64_t K_group, const void* xq,
+                     int64_t m, float* y, q2k_stream_t stream)
+{
+    if (!W || !xq || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (groups <= 0 || groups > 4096 || rows_per_group <= 0 || K_group <= 0 || K_group % kBlockWeights ||
+        K_group > kMaxK || m < 1 || m > 8 || groups * rows_per_group > (1 << 30))
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W, 4) || !aligned(xq, 4) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    MvProblem p{};
+    p.act = ACT_Q8;
+    p.m = (int)m;
+    p.K = K_group;
+    p.n_seg = (int)groups;
+    p.W[0] = W;  // group g: rows g*rows_per_group.. of W
+    p.w_seg_stride = rows_per_group * (int64_t)q2k_row_bytes(K_group);
+    p.N[0] = rows_per_group;
+    p.y_exp = y;  // y[t, g*rows_per_group + r]
+    p.ldy_exp = groups * rows_per_group;
+    p.seg_major = 1;  // each group gets CTAs of its own, its slice staged once
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(groups * K_group);
+    p.x_seg_stride = (int64_t)q8_1_row_bytes(K_group);  // group g's blocks of each token's row
+    return finish(launch_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K, const void* xq,
                      int x_per_matrix, float* y, const float* route_w, float* y_sum, q2k_stream_t stream)
 {

@@ -44,6 +44,10 @@ struct MvProblem {
     // is SwiGLU(gu[e], gu[gu_E + e]) of fp32 rows of length K, quantised per
     // CTA.  x_out, when set, receives the q8_1 rows (row e at e * x_seg_stride).
     int x_prep;
+    // segments as row blocks of one matrix W[0] (table mode without a
+    // pointer table): segment e starts at W[0] + e * w_seg_stride bytes
+    int64_t w_seg_stride;
+    int64_t ldy_exp;  // token stride of y_exp, in floats (several tokens)
     const float* gu;
     int64_t gu_E;
     void* x_out;

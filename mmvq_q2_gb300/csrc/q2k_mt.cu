@@ -711,7 +711,8 @@ bool mt_supported(const MvProblem& p)
 {
     // from the token counts on where it beats the integer-dot kernel
     const int m_min = p.act == ACT_Q8 ? 5 : 3;
-    return p.W_table == nullptr && p.m >= m_min && p.m <= kTok && (p.n_seg == 1 || p.x_seg_stride == 0);
+    return p.W_table == nullptr && p.w_seg_stride == 0 && p.m >= m_min && p.m <= kTok &&
+           (p.n_seg == 1 || p.x_seg_stride == 0);
 }
 
 cudaError_t launch_mt(const MvProblem& p, cudaStream_t s)

@@ -86,6 +86,8 @@ struct MvArgs {
     int64_t x_seg_stride;
     const uint8_t* W[2];
     const void* const* W_table;
+    int64_t w_seg_stride;  // table without W_table: segment e is W[0] + e * w_seg_stride
+    int64_t ldy_exp;       // token stride of y_exp (table outputs for several tokens)
     const float* gu;  // x_prep 2: fp32 gate rows [gu_E][gu_ld], then up rows
     uint8_t* x_out;   // x_prep: the prepared q8_1 rows are also stored here
     int64_t gu_ld;    // floats per gu row
@@ -153,6 +155,8 @@ __device__ __forceinline__ Stage stage_at(const MvArgs& a, int lo, int hi, int i
 __device__ __forceinline__ const uint8_t* seg_weights(const MvArgs& a, int e)
 {
     if (a.table) {
+        if (!a.W_table)  // row blocks of one matrix at a fixed stride
+            return a.W[0] + (int64_t)e * a.w_seg_stride;
         const void* p;
         asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(p) : "l"(a.W_table + e));
         return static_cast<const uint8_t*>(p);
@@ -174,7 +178,10 @@ struct Slice {
 };
 
 // Pack the four group sums of one (token, half) as 16-bit fixed point with
-// a common power-of-two exponent (error below 2^-15 of the largest).
+// a common power-of-two exponent (error below 2^-14 of the largest).  The
+// largest lands below 2^14, so rounding can never reach 2^15 and wrap the
+// 16-bit field (a sum d*S of a q8_1 scale and an integer can sit within
+// half a step of a power of two).
 template <int M, int ACT, int SW>
 __device__ __forceinline__ void pack_sums(Slice<M, ACT, SW>& sl, int t, int hh, const float (&xs)[4])
 {
@@ -185,18 +192,19 @@ __device__ __forceinline__ void pack_sums(Slice<M, ACT, SW>& sl, int t, int hh, 
         sl.xsb[t][hh] = 0.f;
         return;
     }
-    const float scale = __uint_as_float((268u - eb) << 23);  // |xs * scale| < 2^15
+    const float scale = __uint_as_float((267u - eb) << 23);  // |xs * scale| < 2^14
     int q[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         q[j] = __float2int_rn(xs[j] * scale);
     sl.xs16[t][hh][0] = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[1] << 16);
     sl.xs16[t][hh][1] = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
-    sl.xsb[t][hh] = __uint_as_float((eb - 14u) << 23);
+    sl.xsb[t][hh] = __uint_as_float((eb - 13u) << 23);
 }
 
 // 8-word slices: the eight group sums of a token, (j, h) for j = 0..3 and
-// h = 0, 1, as 16-bit fixed point with one power-of-two exponent, packed as
+// h = 0, 1, as 16-bit fixed point with one power-of-two exponent (the
+// largest below 2^14, as in pack_sums), packed as
 // xs16[t][j >> 1][j & 1] = {sum(j, 0), sum(j, 1)}: the order of the min
 // nibbles in the two scale words of a half block.
 template <int M, int ACT, int SW>
@@ -212,14 +220,14 @@ __device__ __forceinline__ void pack_sums8(Slice<M, ACT, SW>& sl, int t, const f
         sl.xsb[t][0] = 0.f;
         return;
     }
-    const float scale = __uint_as_float((268u - eb) << 23);  // |xs * scale| < 2^15
+    const float scale = __uint_as_float((267u - eb) << 23);  // |xs * scale| < 2^14: no wrap
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int q0 = __float2int_rn(xs[0][j] * scale);
         const int q1 = __float2int_rn(xs[1][j] * scale);
         sl.xs16[t][j >> 1][j & 1] = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16);
     }
-    sl.xsb[t][0] = __uint_as_float((eb - 14u) << 23);
+    sl.xsb[t][0] = __uint_as_float((eb - 13u) << 23);
 }
 
 // Bytes of one token's activations per block column in the shared staging
@@ -1036,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1) q2k_mv_kernel(const MvArgs a)
             const int row = st.row0 + rr;
             if (a.table) {
                 if (a.y_exp) {
-                    float* yp = a.y_exp + (int64_t)st.e * a.N[0] + row;
+                    float* yp = a.y_exp + (int64_t)t * a.ldy_exp + (int64_t)st.e * a.N[0] + row;
                     *yp = a.accumulate ? *yp + v : v;
                 }
             } else {
@@ -1149,7 +1157,7 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
     if (err != cudaSuccess)
         return err;
     const int64_t nb = p.K / kBlockWeights;
-    const bool table = p.W_table != nullptr;
+    const bool table = p.W_table != nullptr || p.w_seg_stride != 0;  // segments of one shape
     if (p.N[0] > (1 << 30) || p.N[1] > (1 << 30) || (int64_t)p.N[0] + p.N[1] > (1 << 30))
         return cudaErrorInvalidValue;
 
@@ -1207,6 +1215,8 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
             a.ldy[e] = p.ldy[e];
         }
         a.y_exp = p.y_exp;
+        a.ldy_exp = p.ldy_exp;
+        a.w_seg_stride = p.w_seg_stride;
         a.route_w = p.route_w;
         a.y_sum = p.y_sum;
         a.accumulate = kb0 > 0 ? 1 : 0;

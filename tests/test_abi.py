@@ -82,6 +82,12 @@ def test_mmvq_pair_experts_validation(L):
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 0, None) == 2
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, None, 4, FAKE, 512, FAKE, 1, None) == 1
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, -1, FAKE, 512, FAKE, 1, None) == 2
+    # the grouped MMVQ: groups, rows, K_group (multiple of 256) and m in 1..8
+    assert L.q2k_mmvq_grouped(FAKE, 8, 64, 512, None, 1, FAKE, None) == 1
+    assert L.q2k_mmvq_grouped(FAKE, 0, 64, 512, FAKE, 1, FAKE, None) == 2
+    assert L.q2k_mmvq_grouped(FAKE, 8, 64, 500, FAKE, 1, FAKE, None) == 2
+    assert L.q2k_mmvq_grouped(FAKE, 8, 64, 512, FAKE, 9, FAKE, None) == 2
+    assert L.q2k_mmvq_grouped(P(0x10002), 8, 64, 512, FAKE, 1, FAKE, None) == 3
     # the pair over bf16 rows: the q8_1 destination is required; x is 2-byte aligned
     assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 1, None, None) == 1
     assert L.q2k_mmvq_pair_bf16(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 9, FAKE, None) == 2

@@ -166,6 +166,43 @@ def test_mmvq_q8_1_long_rows_one_token(lib, N, K):
         assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
 
 
+def _q8_rows_at_a_rounding_edge(m, K):
+    """q8_1 rows whose every 32-value block has d = 1285 * 2^-16 (exact in
+    fp16) and one q = 51: a slice's group sum d*51 has the mantissa
+    65535/32768, half a step below a power of two, so packing it with its
+    top at 2^15 would round to 2^15 and wrap the 16-bit field."""
+    nblk = K // 32
+    d = np.float16(1285 * 2.0 ** -16)
+    assert float(d) == 1285 * 2.0 ** -16
+    blk = np.zeros((m, nblk, 36), dtype=np.uint8)
+    blk[:, :, 0:2] = np.frombuffer(d.tobytes(), dtype=np.uint8)
+    blk[:, :, 2:4] = np.frombuffer(np.float16(float(d) * 51).tobytes(), dtype=np.uint8)
+    blk[:, :, 4] = 51
+    return blk.reshape(m, nblk * 36)
+
+
+@pytest.mark.parametrize("m,K", [(1, 4096), (1, 8192), (2, 4096)])
+def test_mmvq_min_sums_at_a_rounding_edge(lib, m, K):
+    N = 96
+    W = synth.q2k_matrix(9, f"edge.{K}", N, K)
+    xq = _q8_rows_at_a_rounding_edge(m, K)
+    y = lib.q2k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= 1e-4
+
+
+def test_grouped_min_sums_at_a_rounding_edge(lib):
+    groups, R, Kg, m = 8, 64, 2048, 8  # eight tokens: the 2-word slices
+    W = synth.q2k_matrix(9, "edge.grp", groups * R, Kg)
+    xq = _q8_rows_at_a_rounding_edge(m, groups * Kg)
+    y = lib.q2k_mmvq_grouped(dev(W), groups, R, Kg, dev(xq)).cpu().numpy()
+    xf = oracle.q8_1_dequant(xq, m, groups * Kg)
+    rb = W.nbytes // (groups * R)
+    for g in range(groups):
+        Wg = np.ascontiguousarray(W.reshape(groups * R, rb)[g * R:(g + 1) * R])
+        ref = oracle.matvec(Wg, R, Kg, np.ascontiguousarray(xf[:, g * Kg:(g + 1) * Kg]))
+        assert rel_err_rows(y[:, g * R:(g + 1) * R], ref) <= 1e-4, g
+
+
 def test_gemv_bf16_unaligned_weights_take_the_copy_path(lib):
     N, K = 21, 4096
     W = synth.q2k_matrix(5, "unal", N, K)
@@ -323,6 +360,34 @@ def test_pair_several_tokens_long_k(lib, m, K):
         refq = oracle.matvec(W, W.shape[0], K, xqf)
         assert rel_err_rows(y.cpu().numpy(), refq) <= 1e-4
         assert rel_err_rows(y.cpu().numpy(), oracle.matvec(W, W.shape[0], K, x_f64(x))) <= TOL_Q8
+
+
+# ---- grouped (block-diagonal) MMVQ: the Q2_K wo_a path ----------------------------
+
+@pytest.mark.parametrize("groups,R,Kg,m", [(8, 512, 2048, 1), (8, 512, 2048, 4), (8, 512, 2048, 8),
+                                           (3, 45, 768, 2), (160, 16, 256, 1)])
+def test_grouped_mmvq(lib, groups, R, Kg, m):
+    """og[t, g*R + r] = o_g . W[g*R + r] against the oracle's projection of
+    each group (the q8_1 values the input rows encode); m = 1 also against
+    single calls on each group's row block, bit for bit.  (3, 45, 768): rows
+    that are not 16-byte aligned; 160 groups: more groups than SMs."""
+    W = synth.q2k_matrix(8, f"grp.{groups}.{R}.{Kg}", groups * R, Kg)
+    x = synth.bf16_normal(8, f"grp.x.{m}.{groups * Kg}", (m, groups * Kg))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q2k_mmvq_grouped(dev(W), groups, R, Kg, dev(xq)).cpu().numpy()
+    xf = oracle.q8_1_dequant(xq, m, groups * Kg)
+    rb = W.nbytes // (groups * R)  # bytes per row
+    for g in range(groups):
+        Wg = W.reshape(groups * R, rb)[g * R:(g + 1) * R]
+        ref = oracle.matvec(np.ascontiguousarray(Wg), R, Kg, np.ascontiguousarray(xf[:, g * Kg:(g + 1) * Kg]))
+        assert rel_err_rows(y[:, g * R:(g + 1) * R], ref) <= 1e-4, g
+    if m == 1:
+        q8b = xq.reshape(-1)
+        for g in sorted({0, groups // 2, groups - 1}):
+            Wg = np.ascontiguousarray(W.reshape(groups * R, rb)[g * R:(g + 1) * R])
+            xg = np.ascontiguousarray(q8b[g * (Kg // 32) * 36:(g + 1) * (Kg // 32) * 36]).reshape(1, -1)
+            single = lib.q2k_mmvq_q8_1(dev(Wg), dev(xg), Kg).cpu().numpy()
+            np.testing.assert_array_equal(y[:, g * R:(g + 1) * R], single)
 
 
 # ---- a6: routed experts -------------------------------------------------------------
