@@ -362,6 +362,29 @@ def test_pair_several_tokens_long_k(lib, m, K):
         assert rel_err_rows(y.cpu().numpy(), oracle.matvec(W, W.shape[0], K, x_f64(x))) <= TOL_Q8
 
 
+# ---- seeded sweep of small problems: every slice width and token count ---------------
+
+@pytest.mark.parametrize("seed", range(24))
+def test_gemv_and_mmvq_seeded_sweep(lib, seed):
+    """Random shapes (1..8 tokens, K from 1 to 40 blocks, ragged N) through
+    both activation types, against the oracle: data-dependent paths (the
+    activation exponents, the 16-bit sums) meet many inputs."""
+    rng = np.random.default_rng(1000 + seed)
+    m = int(rng.integers(1, 9))
+    K = 256 * int(rng.choice([1, 2, 3, 5, 8, 16, 24, 32, 33, 40]))
+    N = int(rng.integers(16, 300))  # enough outputs that the row norm is not one cancelled dot
+    W = synth.q2k_matrix(10 + seed, f"sw.{seed}", N, K)
+    x = synth.bf16_normal(10 + seed, f"sw.x.{seed}", (m, K))
+    if seed % 3 == 0:  # wide dynamic range inside groups
+        v = synth.bf16_bits_to_f32(x) * np.exp2(rng.integers(-12, 12, size=(m, K))).astype(np.float32)
+        x = synth.f32_to_bf16_bits(v)
+    y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+    assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+    xq = oracle.q8_1_quantize(x)
+    yq = lib.q2k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(yq, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= 1e-4
+
+
 # ---- grouped (block-diagonal) MMVQ: the Q2_K wo_a path ----------------------------
 
 @pytest.mark.parametrize("groups,R,Kg,m", [(8, 512, 2048, 1), (8, 512, 2048, 4), (8, 512, 2048, 8),
