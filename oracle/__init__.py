@@ -82,6 +82,9 @@ def _L():
             lib.oracle_swiglu.argtypes = [P, P, I64, P]
             lib.oracle_weighted_sum.argtypes = [P, P, I64, I64, P]
             lib.oracle_round_bf16.argtypes = [P, I64, P]
+            lib.oracle_engram_hash.restype = ctypes.c_int
+            lib.oracle_engram_hash.argtypes = [P, I64, P, I64, P, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               P, P, P, I64, P]
             lib.oracle_block_bytes.restype = ctypes.c_int
             lib.oracle_q8_1_block_bytes.restype = ctypes.c_int
             _lib = lib
@@ -282,3 +285,31 @@ def moe_m1(x_bf16, gate, up, down, route_w, dim, inter, quantized=False):
     dn = np.stack([matvec(down[e], dim, inter, hin[e:e + 1])[0] for e in range(E)])
     y = weighted_sum(dn, route_w)
     return {"g": g, "u": u, "h_bits": h_bits, "down": dn, "y": y}
+
+
+def engram_hash(token_map, cache, input_ids, start_pos, max_ngram, n_layers, n_heads, multipliers, primes,
+                offsets, pad_id):
+    """engram_v41.rs `EngramHasher::hash`: row ids [seqlen, n_layers,
+    (max_ngram-1)*n_heads] (int64); ``cache`` (int64 [max_seq]) is updated in
+    place.  Raises on a token outside token_map or past the cache, as the
+    page does (the cache entries before a bad token are written)."""
+    token_map = _c(token_map, np.int64)
+    assert cache.dtype == np.int64 and cache.flags.c_contiguous
+    ids = _c(input_ids, np.uint32)
+    mults = _c(multipliers, np.int64)
+    pr = _c(primes, np.int64)
+    off = _c(offsets, np.int64)
+    cols = (max_ngram - 1) * n_heads
+    out = np.zeros((len(ids), n_layers, cols), dtype=np.int64)
+    st = _L().oracle_engram_hash(_p(token_map), len(token_map), _p(cache), len(cache), _p(ids), len(ids), start_pos,
+                                 max_ngram, n_layers, n_heads, _p(mults), _p(pr), _p(off), pad_id, _p(out))
+    if st == -1:
+        raise ValueError("token outside the engram token_map")
+    if st == -2:
+        raise ValueError("positions past the hash cache")
+    return out
+
+
+def layer_row_ids(hashes, layer):
+    """engram_v41.rs `layer_row_ids`: one layer's row ids in [token][col] order."""
+    return np.ascontiguousarray(hashes[:, layer, :]).reshape(-1)

@@ -341,5 +341,66 @@ void oracle_round_bf16(const double* v, int64_t n, uint16_t* out)
         out[i] = oracle_f32_to_bf16((float)v[i]);
 }
 
+/* ---- engram n-gram hash ------------------------------------------------
+ * engram_v41.rs, `EngramHasher::hash`: the input tokens are first mapped
+ * through token_map into the sequence cache at start_pos..; then for every
+ * position, the current token and the max_ngram-1 before it (a token before
+ * the sequence start, or any token at or past an unmapped one (-1), reads as
+ * pad_id) are combined per layer by wrapping i64 products and xor, and each
+ * n-gram length i = 1..max_ngram-1 gives n_heads row ids:
+ *   rolling_i = (t_0*mult_0) ^ ... ^ (t_i*mult_i)
+ *   out[s][layer][(i-1)*n_heads + h] = rem_euclid(rolling_i, prime[layer][i-1][h])
+ *                                       + offset[layer][(i-1)*n_heads + h]
+ * Returns 0, -1 for a token id outside token_map (the cache entries before
+ * it are written, as on the page), -2 when the positions pass max_seq. */
+static int64_t wrapping_mul_i64(int64_t a, int64_t b) { return (int64_t)((uint64_t)a * (uint64_t)b); }
+
+static int64_t rem_euclid_i64(int64_t a, int64_t p)
+{
+    int64_t r = a % p;
+    return r < 0 ? r + p : r;
+}
+
+int oracle_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, int64_t max_seq,
+                       const uint32_t* input_ids, int64_t seqlen, int64_t start_pos, int max_ngram,
+                       int n_layers, int n_heads, const int64_t* multipliers, const int64_t* primes,
+                       const int64_t* offsets, int64_t pad_id, int64_t* out)
+{
+    if (start_pos + seqlen > max_seq)
+        return -2;
+    for (int64_t s = 0; s < seqlen; ++s) {
+        if ((int64_t)input_ids[s] >= vocab)
+            return -1;
+        cache[start_pos + s] = token_map[input_ids[s]];
+    }
+    const int cols = (max_ngram - 1) * n_heads;
+    int64_t tokens[64];
+    if (max_ngram > 64)
+        return -2;
+    for (int64_t s = 0; s < seqlen; ++s) {
+        const int64_t pos = start_pos + s;
+        int blocked = 0;
+        for (int shift = 0; shift < max_ngram; ++shift) {
+            const int64_t src = cache[pos >= shift ? pos - shift : 0];
+            blocked = blocked || pos < shift || src == -1;
+            tokens[shift] = blocked ? pad_id : src;
+        }
+        for (int li = 0; li < n_layers; ++li) {
+            const int64_t* mults = multipliers + (int64_t)li * max_ngram;
+            int64_t rolling = wrapping_mul_i64(tokens[0], mults[0]);
+            for (int i = 1; i < max_ngram; ++i) {
+                rolling ^= wrapping_mul_i64(tokens[i], mults[i]);
+                for (int h = 0; h < n_heads; ++h) {
+                    const int col = (i - 1) * n_heads + h;
+                    const int64_t prime = primes[((int64_t)li * (max_ngram - 1) + (i - 1)) * n_heads + h];
+                    out[(s * n_layers + li) * cols + col] =
+                        rem_euclid_i64(rolling, prime) + offsets[(int64_t)li * cols + col];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 int oracle_block_bytes(void) { return Q2K_BYTES; }
 int oracle_q8_1_block_bytes(void) { return Q8_1_BYTES; }

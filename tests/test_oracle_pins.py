@@ -370,3 +370,66 @@ def test_moe_chain_single_expert_and_quantised_agreement():
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
     q = oracle.moe_m1(x, gate, up, down, w, dim, inter, quantized=True)["y"]
     assert np.max(np.abs(q - a)) / np.linalg.norm(a) < 1e-2
+
+
+# ---- engram n-gram hash (engram_v41.rs, EngramHasher::hash) ---------------------
+
+_HASH_ARGS = dict(max_ngram=3, n_layers=2, n_heads=2,
+                  multipliers=np.array([[3, 5, 7], [11, 13, 17]], dtype=np.int64),
+                  primes=np.array([[[101, 103], [107, 109]], [[113, 127], [131, 137]]], dtype=np.int64),
+                  offsets=np.zeros((2, 4), dtype=np.int64), pad_id=0)
+
+
+def test_engram_hash_hand_computed():
+    # token_map[i] = 3i + 1; tokens 5, 7, 9 -> 16, 22, 28; pad 0.
+    # pos 0: [16, pad, pad]: 16*3 = 48 for both lengths.
+    # pos 1: [22, 16, pad]: 66 ^ 80 = 18.
+    # pos 2: [28, 22, 16]: 84 ^ 110 = 58, then 58 ^ 112 = 74.
+    tm = np.arange(100, dtype=np.int64) * 3 + 1
+    out = oracle.engram_hash(tm, np.zeros(8, np.int64), [5, 7, 9], 0, **_HASH_ARGS)
+    np.testing.assert_array_equal(out[:, 0, :], [[48, 48, 48, 48], [18, 18, 18, 18], [58, 58, 74, 74]])
+    # layer 1, pos 0: 16*11 = 176 -> 176 mod 113 = 63, mod 127 = 49, mod 131 = 45, mod 137 = 39
+    np.testing.assert_array_equal(out[0, 1, :], [63, 49, 45, 39])
+
+
+def test_engram_hash_wrapping_products_and_euclidean_remainder():
+    # 2^62 * 2 wraps to -2^63: the remainder is the Euclidean one, in [0, p)
+    tm = np.array([1 << 62], dtype=np.int64)
+    args = dict(_HASH_ARGS, max_ngram=2, n_layers=1, n_heads=1, multipliers=np.array([[2, 0]], np.int64),
+                primes=np.array([[[101]]], np.int64), offsets=np.array([[7]], np.int64))
+    out = oracle.engram_hash(tm, np.zeros(4, np.int64), [0], 0, **args)
+    assert out[0, 0, 0] == 7 + (101 - pow(2, 63, 101)) % 101
+    # 2^62 * 4 wraps to 0
+    args["multipliers"] = np.array([[4, 0]], np.int64)
+    assert oracle.engram_hash(tm, np.zeros(4, np.int64), [0], 0, **args)[0, 0, 0] == 7
+
+
+def test_engram_hash_ranges_blocking_and_incremental_calls():
+    rng = np.random.default_rng(5)
+    tm = rng.integers(0, 1 << 40, size=500).astype(np.int64)
+    tm[13] = -1  # an unmapped token blocks every shift that reaches it
+    args = dict(_HASH_ARGS, max_ngram=4, n_layers=2, n_heads=3,
+                multipliers=rng.integers(-(1 << 62), 1 << 62, size=(2, 4)).astype(np.int64),
+                primes=rng.integers(1000, 1 << 30, size=(2, 3, 3)).astype(np.int64),
+                offsets=rng.integers(0, 1 << 20, size=(2, 9)).astype(np.int64), pad_id=99)
+    ids = rng.integers(0, 500, size=12).astype(np.uint32)
+    ids[6] = 13
+    out = oracle.engram_hash(tm, np.zeros(16, np.int64), ids, 0, **args)
+    lo = args["offsets"][None, :, :]
+    hi = lo + np.repeat(args["primes"].reshape(2, 3, 3), 1, axis=1).reshape(2, 9)[None]
+    assert np.all(out >= lo) and np.all(out < hi)
+    # positions 6..8 see the unmapped token at shift pos-6: shifts from there on read pad,
+    # so pos 6 equals the hash of an all-pad n-gram
+    pad_only = oracle.engram_hash(np.array([99], np.int64), np.zeros(4, np.int64), [0], 0, **args)
+    np.testing.assert_array_equal(out[6], pad_only[0])
+    # the cache carries the sequence: one call of 12 equals calls of 5 and 7
+    cache = np.zeros(16, np.int64)
+    a = oracle.engram_hash(tm, cache, ids[:5], 0, **args)
+    b = oracle.engram_hash(tm, cache, ids[5:], 5, **args)
+    np.testing.assert_array_equal(np.concatenate([a, b]), out)
+    # errors as on the page
+    with pytest.raises(ValueError):
+        oracle.engram_hash(tm, np.zeros(16, np.int64), [600], 0, **args)
+    with pytest.raises(ValueError):
+        oracle.engram_hash(tm, np.zeros(4, np.int64), ids[:5], 0, **args)
+    np.testing.assert_array_equal(oracle.layer_row_ids(out, 1), out[:, 1, :].reshape(-1))
