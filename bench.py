@@ -461,7 +461,7 @@ def sweep(q, L, l2, hbm, rank):
     el, n = graph_time(lambda i: check(L.q2k_moe_m1(P(tables[i % 64]), topk, dim, inter, P(xd), P(wd), P(yo), P(ws),
                                                     wsb, cur()), "moe"), 1000, 50)
     moe_bytes = 3 * topk * inter * (dim // 256) * 84
-    rec("moe_m1 (8 of 256 experts, gate/up -> SwiGLU -> down)", el / n, moe_bytes, 1, {"launches_per_call": 4})
+    rec("moe_m1 (8 of 256 experts, gate/up -> SwiGLU -> down)", el / n, moe_bytes, 1, {"launches_per_call": 3})
     del mats, tables
     torch.cuda.empty_cache()
 
@@ -481,6 +481,27 @@ def sweep(q, L, l2, hbm, rank):
     el, n = graph_time(engram, 500, 20)
     rec("engram rows(128) + dense_gemm m=16 [20480x2048]", el / n, wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 +
         16 * 20480 * 4, 16)
+
+    # the engram chain on the device: n-gram hash of 16 tokens (3-grams, 2 layers, 4 heads) -> one
+    # layer's 128 row ids -> rows -> the m = 16 GEMM (no host round trip)
+    rng = np.random.default_rng(0)
+    tm = torch.from_numpy(rng.integers(0, 1 << 40, size=1 << 16).astype(np.int64)).cuda()
+    hc = torch.zeros(4096, dtype=torch.int64, device="cuda")
+    toks = torch.from_numpy(rng.integers(0, 1 << 16, size=16).astype(np.uint32)).cuda()
+    mults = torch.from_numpy(rng.integers(-(1 << 62), 1 << 62, size=(2, 3)).astype(np.int64)).cuda()
+    primes = torch.full((2, 2, 4), 131071, dtype=torch.int64, device="cuda")
+    offs = torch.from_numpy((np.arange(16, dtype=np.int64) % 8 * 65536).reshape(2, 8)).cuda()  # ids < 2^20
+    hout = torch.empty((16, 2, 8), dtype=torch.int64, device="cuda")
+    lids = torch.empty((16, 8), dtype=torch.int32, device="cuda")
+
+    def engram_chain(i):
+        check(L.q2k_engram_hash(P(tm), tm.numel(), P(hc), hc.numel(), P(toks), 16, 0, 3, 2, 4, P(mults), P(primes),
+                                P(offs), 0, P(hout), P(lids), 1, None, cur()), "hash")
+        check(L.q2k_dequant_rows(P(table), n_table, 256, P(lids), 128, P(rows), None, cur()), "dequant")
+        check(L.dense_gemm_bf16(P(rows), 16, 2048, 2048, P(wkvs[i % R]), 20480, P(yk), 20480, cur()), "gemm")
+    el, n = graph_time(engram_chain, 500, 20)
+    rec("engram hash(16 tok) + rows(128) + dense_gemm m=16 [20480x2048]", el / n,
+        wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 + 16 * 20480 * 4, 16)
     del wkvs
 
     # cfg4: dense GEMM m in {64, 256}

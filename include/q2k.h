@@ -91,6 +91,38 @@ size_t q8_1_row_bytes(int64_t K);
 int q2k_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const int32_t* ids,
                      int64_t n_rows, uint16_t* out_bf16, int32_t* err_flag, q2k_stream_t stream);
 
+/* Engram n-gram hash on the device (engram_v41.rs, `EngramHasher::hash`):
+ * the ids of the engram table rows for a run of tokens, so that the rows can
+ * be gathered (q2k_dequant_rows) and projected without a host round trip.
+ *   token_map    int64 [vocab]: token id -> engram token (-1: unmapped)
+ *   cache        int64 [max_seq]: the sequence's mapped tokens; positions
+ *                start_pos .. start_pos+seqlen-1 are written, earlier ones
+ *                are read (the caller keeps it across calls, as the page's
+ *                hasher keeps its cache)
+ *   input_ids    uint32 [seqlen]
+ *   multipliers  int64 [n_layers, max_ngram]
+ *   primes       int64 [n_layers, max_ngram-1, n_heads] (positive)
+ *   offsets      int64 [n_layers, (max_ngram-1)*n_heads]
+ *   out          int64 [seqlen, n_layers, cols], cols = (max_ngram-1)*n_heads:
+ *                rolling_i = (t_0*m_0) ^ ... ^ (t_i*m_i) over the current
+ *                token and the i before it (wrapping i64 products; a token
+ *                before the start, or at or past an unmapped one, reads as
+ *                pad_id); out[s, l, (i-1)*n_heads + h] =
+ *                rem_euclid(rolling_i, primes[l, i-1, h]) + offsets[l, col]
+ *   layer_ids    int32 [seqlen, cols], nullable: layer layer_index's ids in
+ *                [token][col] order (`layer_row_ids`), ready for
+ *                q2k_dequant_rows
+ *   err_flag     int32, nullable: bit 0 set when an input id is outside
+ *                token_map (that position then reads as unmapped; the page
+ *                stops with an error instead), bit 1 when a prime is not
+ *                positive (its ids are 0)
+ * 2 <= max_ngram <= 16; start_pos + seqlen <= max_seq.  One launch. */
+int q2k_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, int64_t max_seq,
+                    const uint32_t* input_ids, int64_t seqlen, int64_t start_pos, int64_t max_ngram,
+                    int64_t n_layers, int64_t n_heads, const int64_t* multipliers, const int64_t* primes,
+                    const int64_t* offsets, int64_t pad_id, int64_t* out, int32_t* layer_ids,
+                    int64_t layer_index, int32_t* err_flag, q2k_stream_t stream);
+
 /* Quantise bf16 rows to q8_1 (attn_v41/decode.rs, `kquant_q8_1_rows`;
  * moe_v41/init.rs, `kquant_q8_1_rows_bf16`).
  *   x_bf16   [m, K] with row stride ldx elements (ldx >= K); K % 32 == 0

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libq2k.so")
 
 # Every entry point include/q2k.h declares.
 EXPORTS = (
-    "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16",
+    "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q2k_engram_hash", "q8_1_quantize_rows",
+    "q2k_gemv_bf16",
     "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_grouped", "q2k_mmvq_experts",
     "swiglu_q8_1_rows",
     "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "q8_1_row_bytes": (SZ, [I64]),
             "q2k_dequant_rows": (I32, [P, I64, I64, P, I64, P, P, P]),
             "q8_1_quantize_rows": (I32, [P, I64, I64, I64, P, P]),
+            "q2k_engram_hash": (I32, [P, I64, P, I64, P, I64, I64, I64, I64, I64, P, P, P, I64, P, P, I64, P, P]),
             "q2k_gemv_bf16": (I32, [P, I64, I64, P, I64, I64, P, I64, P]),
             "q2k_mmvq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P]),
             "q2k_mmvq_pair": (I32, [P, I64, P, P, I64, P, I64, P, I64, P]),
@@ -131,6 +133,22 @@ def q2k_dequant_rows(table, K, ids=None, n_rows=None, out=None, err_flag=None, s
     _call("q2k_dequant_rows", _ptr(table), n_table_rows, K, _ptr(ids), n_rows, _ptr(out), _ptr(err_flag),
           _stream(stream))
     return out
+
+
+def q2k_engram_hash(token_map, cache, input_ids, start_pos, max_ngram, n_layers, n_heads, multipliers, primes,
+                    offsets, pad_id, layer_index=None, err_flag=None, stream=None):
+    """Engram row ids of ``input_ids`` at ``start_pos`` -> (out int64
+    ``[seqlen, n_layers, cols]``, layer ids int32 ``[seqlen, cols]`` or
+    None); ``cache`` is updated on the device."""
+    _need_cuda(token_map, cache, input_ids, multipliers, primes, offsets, err_flag)
+    seqlen = input_ids.numel()
+    cols = (max_ngram - 1) * n_heads
+    out = torch.empty((seqlen, n_layers, cols), dtype=torch.int64, device=cache.device)
+    lids = None if layer_index is None else torch.empty((seqlen, cols), dtype=torch.int32, device=cache.device)
+    _call("q2k_engram_hash", _ptr(token_map), token_map.numel(), _ptr(cache), cache.numel(), _ptr(input_ids), seqlen,
+          start_pos, max_ngram, n_layers, n_heads, _ptr(multipliers), _ptr(primes), _ptr(offsets), pad_id, _ptr(out),
+          _ptr(lids), -1 if layer_index is None else layer_index, _ptr(err_flag), _stream(stream))
+    return out, lids
 
 
 def q8_1_quantize_rows(x, out=None, stream=None):

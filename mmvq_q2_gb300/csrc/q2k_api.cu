@@ -153,6 +153,33 @@ int q2k_dequant_rows(const void* table, int64_t n_table_rows, int64_t K, const i
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int q2k_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, int64_t max_seq,
+                    const uint32_t* input_ids, int64_t seqlen, int64_t start_pos, int64_t max_ngram,
+                    int64_t n_layers, int64_t n_heads, const int64_t* multipliers, const int64_t* primes,
+                    const int64_t* offsets, int64_t pad_id, int64_t* out, int32_t* layer_ids,
+                    int64_t layer_index, int32_t* err_flag, q2k_stream_t stream)
+{
+    if (!token_map || !cache || (seqlen > 0 && !input_ids) || !multipliers || !primes || !offsets ||
+        (seqlen > 0 && !out))
+        return Q2K_ERR_NULL_ARG;
+    if (vocab <= 0 || max_seq <= 0 || seqlen < 0 || start_pos < 0 || start_pos + seqlen > max_seq ||
+        max_ngram < 2 || max_ngram > 16 || n_layers < 1 || n_layers > 1024 || n_heads < 1 || n_heads > 1024 ||
+        (layer_ids && (layer_index < 0 || layer_index >= n_layers)))
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(token_map, 8) || !aligned(cache, 8) || !aligned(input_ids, 4) || !aligned(multipliers, 8) ||
+        !aligned(primes, 8) || !aligned(offsets, 8) || !aligned(out, 8) || !aligned(layer_ids, 4) ||
+        !aligned(err_flag, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (seqlen == 0)
+        return Q2K_OK;
+    return finish(launch_engram_hash(token_map, vocab, cache, input_ids, seqlen, start_pos, (int)max_ngram,
+                                     (int)n_layers, (int)n_heads, multipliers, primes, offsets, pad_id, out, layer_ids,
+                                     (int)layer_index, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx, void* out_q8_1,
                        q2k_stream_t stream)
 {

@@ -64,6 +64,10 @@ cudaError_t launch_q8_1_quantize(const uint16_t* x, int64_t m, int64_t K, int64_
                                  cudaStream_t s);
 cudaError_t launch_swiglu_q8_1(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16,
                                cudaStream_t s);
+cudaError_t launch_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, const uint32_t* input_ids,
+                               int64_t seqlen, int64_t start_pos, int ng, int nl, int nh, const int64_t* mults,
+                               const int64_t* primes, const int64_t* offsets, int64_t pad_id, int64_t* out,
+                               int32_t* layer_ids, int layer_index, int32_t* err_flag, cudaStream_t s);
 // y_sum[n] = sum_e route_w[e] * y_exp[e][n], fp32 fmaf in e order from 0.
 cudaError_t launch_expert_sum(const float* y_exp, const float* route_w, int64_t E, int64_t N, float* y_sum,
                               cudaStream_t s);

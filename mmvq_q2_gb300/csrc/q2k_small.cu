@@ -209,4 +209,89 @@ cudaError_t launch_expert_sum(const float* y_exp, const float* route_w, int64_t 
     return launch_pdl(expert_sum_kernel, dim3((unsigned)grid), dim3(256), 0, s, y_exp, route_w, (int)E, N, y_sum);
 }
 
+// ---- engram n-gram hash ---------------------------------------------------------
+// engram_v41.rs, `EngramHasher::hash`, on the device: the input tokens are
+// mapped through token_map into the sequence cache at start_pos.., then for
+// each position and layer the n-gram chain rolling_i = (t_0*m_0) ^ ... ^
+// (t_i*m_i) (wrapping i64 products) gives, per n-gram length i and head h,
+// rem_euclid(rolling_i, prime) + offset.  A token before the sequence start,
+// or at or past an unmapped one (-1), reads as pad_id.
+constexpr int kHashMaxNgram = 16;
+
+// Mapped token at sequence position pos: this call's tokens are read through
+// token_map directly (so no thread waits for another's cache write), earlier
+// ones from the cache.  An id outside token_map reads as unmapped (-1).
+__device__ __forceinline__ int64_t hash_token_at(const int64_t* token_map, int64_t vocab, const int64_t* cache,
+                                                 const uint32_t* input_ids, int64_t start_pos, int64_t pos)
+{
+    if (pos < start_pos)
+        return cache[pos];
+    const uint32_t id = input_ids[pos - start_pos];
+    return (int64_t)id < vocab ? token_map[id] : -1;
+}
+
+__global__ void __launch_bounds__(256) engram_hash_kernel(
+    const int64_t* __restrict__ token_map, int64_t vocab, int64_t* __restrict__ cache,
+    const uint32_t* __restrict__ input_ids, int64_t seqlen, int64_t start_pos, int ng, int nl, int nh,
+    const int64_t* __restrict__ mults, const int64_t* __restrict__ primes, const int64_t* __restrict__ offsets,
+    int64_t pad_id, int64_t* __restrict__ out, int32_t* __restrict__ layer_ids, int layer_index,
+    int32_t* __restrict__ err_flag)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // this call's tokens into the cache (read by later calls)
+    for (int64_t s = t0; s < seqlen; s += stride) {
+        const uint32_t id = input_ids[s];
+        if ((int64_t)id >= vocab && err_flag)
+            atomicOr(err_flag, 1);  // outside token_map: the position reads as unmapped
+        cache[start_pos + s] = (int64_t)id < vocab ? token_map[id] : -1;
+    }
+    // one thread per output id (position s, layer li, column col = (i-1)*nh + h)
+    const int cols = (ng - 1) * nh;
+    for (int64_t u = t0; u < seqlen * nl * cols; u += stride) {
+        const int64_t s = u / ((int64_t)nl * cols);
+        const int rem = (int)(u - s * nl * cols);
+        const int li = rem / cols, col = rem - li * cols;
+        const int i = col / nh + 1, h = col - (i - 1) * nh;  // n-gram of the token and the i before it
+        const int64_t pos = start_pos + s;
+        const int64_t* m = mults + (int64_t)li * ng;
+        bool blocked = false;
+        uint64_t rolling = 0;
+#pragma unroll
+        for (int shift = 0; shift < kHashMaxNgram; ++shift) {
+            if (shift <= i) {
+                int64_t t = -1;
+                if (pos >= shift)
+                    t = hash_token_at(token_map, vocab, cache, input_ids, start_pos, pos - shift);
+                blocked = blocked || pos < shift || t == -1;
+                rolling ^= (uint64_t)(blocked ? pad_id : t) * (uint64_t)m[shift];
+            }
+        }
+        const int64_t p = primes[((int64_t)li * (ng - 1) + (i - 1)) * nh + h];
+        int64_t v = 0;
+        if (p > 0) {
+            const int64_t r = (int64_t)rolling % p;
+            v = (r < 0 ? r + p : r) + offsets[(int64_t)li * cols + col];
+        } else if (err_flag) {
+            atomicOr(err_flag, 2);  // a modulus that is not positive: id 0
+        }
+        out[u] = v;
+        if (layer_ids && li == layer_index)
+            layer_ids[s * cols + col] = (int32_t)v;
+    }
+}
+
+cudaError_t launch_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, const uint32_t* input_ids,
+                               int64_t seqlen, int64_t start_pos, int ng, int nl, int nh, const int64_t* mults,
+                               const int64_t* primes, const int64_t* offsets, int64_t pad_id, int64_t* out,
+                               int32_t* layer_ids, int layer_index, int32_t* err_flag, cudaStream_t s)
+{
+    const int64_t work = std::max<int64_t>(seqlen, seqlen * nl * (int64_t)(ng - 1) * nh);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 1024));
+    return launch_pdl(engram_hash_kernel, dim3((unsigned)grid), dim3(256), 0, s, token_map, vocab, cache, input_ids, seqlen,
+                      start_pos, ng, nl, nh, mults, primes, offsets, pad_id, out, layer_ids, layer_index, err_flag);
+}
+
 }  // namespace q2k

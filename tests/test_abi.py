@@ -82,6 +82,19 @@ def test_mmvq_pair_experts_validation(L):
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, 4, FAKE, 512, FAKE, 0, None) == 2
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, None, 4, FAKE, 512, FAKE, 1, None) == 1
     assert L.q2k_mmvq_pair(FAKE, 4, FAKE, FAKE, -1, FAKE, 512, FAKE, 1, None) == 2
+    # the engram hash: positions within the cache, 2 <= max_ngram <= 16, a layer in range
+    H = lambda *a: L.q2k_engram_hash(*a)  # noqa: E731
+    ok = (FAKE, 100, FAKE, 64, FAKE, 4, 0, 3, 2, 2, FAKE, FAKE, FAKE, 0, FAKE, None, 0, None, None)
+    bad = list(ok); bad[0] = None
+    assert H(*bad) == 1
+    bad = list(ok); bad[6] = 61  # start_pos + seqlen > max_seq
+    assert H(*bad) == 2
+    bad = list(ok); bad[7] = 17
+    assert H(*bad) == 2
+    bad = list(ok); bad[15] = FAKE; bad[16] = 2  # layer_index outside n_layers
+    assert H(*bad) == 2
+    bad = list(ok); bad[2] = P(0x10004)  # cache not 8-byte aligned
+    assert H(*bad) == 3
     # the grouped MMVQ: groups, rows, K_group (multiple of 256) and m in 1..8
     assert L.q2k_mmvq_grouped(FAKE, 8, 64, 512, None, 1, FAKE, None) == 1
     assert L.q2k_mmvq_grouped(FAKE, 0, 64, 512, FAKE, 1, FAKE, None) == 2

@@ -106,6 +106,77 @@ def test_dequant_rows_odd_widths_and_unaligned_output(lib, K):
     np.testing.assert_array_equal(host_bits(out.contiguous()), ref)
 
 
+def _hash_setup(seed, ng=3, nl=2, nh=4, vocab=1000):
+    rng = np.random.default_rng(seed)
+    tm = rng.integers(0, 1 << 40, size=vocab).astype(np.int64)
+    tm[rng.integers(0, vocab, size=5)] = -1
+    args = dict(max_ngram=ng, n_layers=nl, n_heads=nh,
+                multipliers=rng.integers(-(1 << 62), 1 << 62, size=(nl, ng)).astype(np.int64),
+                primes=rng.integers(1 << 19, 1 << 20, size=(nl, ng - 1, nh)).astype(np.int64),
+                offsets=(np.arange(nl * (ng - 1) * nh, dtype=np.int64) * (1 << 20)).reshape(nl, -1),
+                pad_id=int(rng.integers(0, 1 << 40)))
+    return rng, tm, args
+
+
+def _hash_dev(lib, tm, cache_d, ids, start, args, layer_index=None, err=None):
+    return lib.q2k_engram_hash(dev(tm), cache_d, dev(np.asarray(ids, np.uint32)), start, args["max_ngram"],
+                               args["n_layers"], args["n_heads"], dev(args["multipliers"]), dev(args["primes"]),
+                               dev(args["offsets"]), args["pad_id"], layer_index=layer_index, err_flag=err)
+
+
+@pytest.mark.parametrize("ng,nl,nh,seqlen", [(3, 2, 4, 16), (2, 1, 1, 1), (16, 3, 2, 700)])
+def test_engram_hash_against_oracle_and_incremental(lib, ng, nl, nh, seqlen):
+    rng, tm, args = _hash_setup(ng * 100 + seqlen, ng, nl, nh)
+    ids = rng.integers(0, len(tm), size=seqlen).astype(np.uint32)
+    cache = np.zeros(seqlen + 8, np.int64)
+    ref = oracle.engram_hash(tm, cache, ids, 0, **args)
+    cache_d = torch.zeros(seqlen + 8, dtype=torch.int64, device="cuda")
+    out, lid = _hash_dev(lib, tm, cache_d, ids, 0, args, layer_index=nl - 1)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+    np.testing.assert_array_equal(lid.cpu().numpy().reshape(-1), oracle.layer_row_ids(ref, nl - 1).astype(np.int32))
+    np.testing.assert_array_equal(cache_d.cpu().numpy(), cache)
+    # the same tokens in two calls (decode: one at a time after a prefix)
+    cut = seqlen // 2
+    c2 = torch.zeros(seqlen + 8, dtype=torch.int64, device="cuda")
+    a, _ = _hash_dev(lib, tm, c2, ids[:cut], 0, args)
+    b, _ = _hash_dev(lib, tm, c2, ids[cut:], cut, args)
+    np.testing.assert_array_equal(np.concatenate([a.cpu().numpy(), b.cpu().numpy()]), ref)
+
+
+def test_engram_hash_token_outside_the_map_sets_the_flag(lib):
+    rng, tm, args = _hash_setup(7)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache_d = torch.zeros(8, dtype=torch.int64, device="cuda")
+    out, _ = _hash_dev(lib, tm, cache_d, [3, len(tm) + 5, 4], 0, args, err=err)
+    assert err.item() & 1
+    assert cache_d[1].item() == -1  # reads as unmapped: later n-grams that reach it see pad
+    tm2 = tm.copy()
+    tm2[999] = -1
+    ref = oracle.engram_hash(tm2, np.zeros(8, np.int64), [3, 999, 4], 0, **args)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+def test_engram_hash_rows_projection_chain(lib):
+    """hash -> one layer's ids -> q2k_dequant_rows -> dense GEMM, all on the
+    device, against the oracle's chain (cfg1 shapes: 16 tokens x 8 cols)."""
+    rng, tm, args = _hash_setup(11, ng=3, nl=2, nh=4)
+    n_table = 1 << 20
+    args["primes"] = np.full((2, 2, 4), 131071, np.int64)  # ids inside the table
+    args["offsets"] = (np.arange(16, dtype=np.int64) % 8 * 65536).reshape(2, 8)  # ids below 2^20
+    ids = rng.integers(0, len(tm), size=16).astype(np.uint32)
+    ref_hash = oracle.engram_hash(tm, np.zeros(32, np.int64), ids, 0, **args)
+    row_ids = oracle.layer_row_ids(ref_hash, 1).astype(np.int32)
+    assert row_ids.max() < n_table
+    table = synth.q2k_blocks(0, "cfg1.table", n_table)
+    wkv = synth.bf16_normal(0, "cfg1.wkv", (4096, 2048), std=0.02)
+    _, lid = _hash_dev(lib, tm, torch.zeros(32, dtype=torch.int64, device="cuda"), ids, 0, args, layer_index=1)
+    rows = lib.q2k_dequant_rows(dev(table), 256, ids=lid.view(-1))
+    y = lib.dense_gemm_bf16(rows.view(16, 2048), bf16_dev(wkv)).cpu().numpy()
+    ref_rows, ref_y = oracle.engram_rows_projection(table, n_table, row_ids, 16, 8, wkv)
+    np.testing.assert_array_equal(host_bits(rows), ref_rows)
+    assert rel_err_rows(y, ref_y) <= TOL_BF16
+
+
 # ---- a2: q8_1 ------------------------------------------------------------------
 
 @pytest.mark.parametrize("m,K,pad", [(1, 32, 0), (3, 256, 8), (8, 4096, 0), (2, 16384, 32), (5, 2048, 0)])
