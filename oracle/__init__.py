@@ -85,6 +85,10 @@ def _L():
             lib.oracle_engram_hash.restype = ctypes.c_int
             lib.oracle_engram_hash.argtypes = [P, I64, P, I64, P, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                P, P, P, I64, P]
+            lib.oracle_q3k_decode_block.argtypes = [P, P]
+            lib.oracle_q3k_decode_matrix.argtypes = [P, I64, I64, P]
+            lib.oracle_q3k_matvec.argtypes = [P, I64, I64, P, I64, P]
+            lib.oracle_q3k_block_bytes.restype = ctypes.c_int
             lib.oracle_block_bytes.restype = ctypes.c_int
             lib.oracle_q8_1_block_bytes.restype = ctypes.c_int
             _lib = lib
@@ -179,6 +183,46 @@ def matvec(W: np.ndarray, N: int, K: int, x: np.ndarray) -> np.ndarray:
     assert x.shape[1] == K
     y = np.empty((m, N), dtype=np.float64)
     _L().oracle_q2k_matvec(_p(W), N, K, _p(x), m, _p(y))
+    return y
+
+
+# ---- Q3_K (moe_v41/init.rs names the kernels; the layout is GGUF's, a reading) ----
+
+Q3K_BYTES = 110
+
+
+def q3k_block_bytes() -> int:
+    return _L().oracle_q3k_block_bytes()
+
+
+def q3k_decode_block(blk: np.ndarray) -> np.ndarray:
+    """Exact fp64 weights of one 110-byte Q3_K block
+    (hmask[32] | qs[64] | scales[12] | d)."""
+    blk = _c(blk, np.uint8).reshape(Q3K_BYTES)
+    out = np.empty(Q2K_WEIGHTS, dtype=np.float64)
+    _L().oracle_q3k_decode_block(_p(blk), _p(out))
+    return out
+
+
+def q3k_decode_matrix(W: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Exact fp64 ``[N, K]`` expansion of a Q3_K matrix (``[out, in/256]``
+    blocks, row-major)."""
+    W = _c(W, np.uint8)
+    assert W.size == N * (K // Q2K_WEIGHTS) * Q3K_BYTES
+    out = np.empty((N, K), dtype=np.float64)
+    _L().oracle_q3k_decode_matrix(_p(W), N, K, _p(out))
+    return out
+
+
+def q3k_matvec(W: np.ndarray, N: int, K: int, x: np.ndarray) -> np.ndarray:
+    """``y[t, n] = sum_k w[n, k] x[t, k]`` with exact Q3_K weights, fp64
+    (moe_v41/init.rs, `kquant_mmvq_q3_k_w`).  ``x`` fp64 ``[m, K]``."""
+    W = _c(W, np.uint8)
+    x = _c(np.atleast_2d(x), np.float64)
+    m = x.shape[0]
+    assert x.shape[1] == K and W.size == N * (K // Q2K_WEIGHTS) * Q3K_BYTES
+    y = np.empty((m, N), dtype=np.float64)
+    _L().oracle_q3k_matvec(_p(W), N, K, _p(x), m, _p(y))
     return y
 
 

@@ -242,6 +242,74 @@ void oracle_q2k_matvec(const uint8_t* W, int64_t N, int64_t K, const double* x, 
     }
 }
 
+/* ---- Q3_K ------------------------------------------------------------------ */
+/* moe_v41/init.rs, `MoeV41::new`, names Q3_K twins of the single-matrix and
+ * experts MMVQ kernels; the pages give no Q3_K layout.  Reading: GGUF's
+ * Q3_K, 110 bytes per 256 weights:
+ *   hmask[32] | qs[64] | scales[12] | d (fp16 LE).
+ * Weight p lies in sub-block j = p/16 with a signed 6-bit scale (stored + 32):
+ * low nibble in scales[j] (j < 8) or the high nibble of scales[j-8]
+ * (j >= 8); the top two bits at bit 2*(j/4) of scales[8 + j%4].  Its code is
+ * the 2-bit field laid out as in Q2_K (at byte 32 of the block) minus 4,
+ * unless bit p/32 of hmask[p%32] is set.  w_p = d * scale_j * code_p. */
+#define Q3K_BYTES 110
+
+static int q3k_scale(const uint8_t* sc, int j)
+{
+    int low = j < 8 ? (sc[j] & 15) : (sc[j - 8] >> 4);
+    int high = (sc[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return (low | (high << 4)) - 32;
+}
+
+static int q3k_code(const uint8_t* blk, int p)
+{
+    const uint8_t* hmask = blk;
+    const uint8_t* qs = blk + 32;
+    int lo = (qs[32 * (p / 128) + (p % 32)] >> (2 * ((p % 128) / 32))) & 3;
+    int hi = (hmask[p % 32] >> (p / 32)) & 1;
+    return hi ? lo : lo - 4;
+}
+
+/* Exact decoded weights of one 110-byte block (d * integer in [-128, 128]). */
+void oracle_q3k_decode_block(const uint8_t* blk, double* w)
+{
+    double d = oracle_fp16_to_double(rd16(blk + 108));
+    for (int p = 0; p < Q2K_WEIGHTS; ++p)
+        w[p] = d * (double)q3k_scale(blk + 96, p / 16) * (double)q3k_code(blk, p);
+}
+
+/* Exact decoded matrix [N, K] (fp64). */
+void oracle_q3k_decode_matrix(const uint8_t* W, int64_t N, int64_t K, double* out)
+{
+    int64_t nb = K / Q2K_WEIGHTS;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_q3k_decode_block(W + (n * nb + b) * Q3K_BYTES, out + n * K + b * Q2K_WEIGHTS);
+}
+
+/* y[t, n] = sum_k w[n, k] * x[t, k] for a Q3_K W [N, K]; fp64, k order. */
+void oracle_q3k_matvec(const uint8_t* W, int64_t N, int64_t K, const double* x, int64_t m,
+                       double* y)
+{
+    int64_t nb = K / Q2K_WEIGHTS;
+    double w[Q2K_WEIGHTS];
+    for (int64_t t = 0; t < m; ++t)
+        for (int64_t n = 0; n < N; ++n)
+            y[t * N + n] = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < nb; ++b) {
+            oracle_q3k_decode_block(W + (n * nb + b) * Q3K_BYTES, w);
+            for (int64_t t = 0; t < m; ++t) {
+                double acc = 0.0;
+                const double* xr = x + t * K + b * Q2K_WEIGHTS;
+                for (int p = 0; p < Q2K_WEIGHTS; ++p)
+                    acc += w[p] * xr[p];
+                y[t * N + n] += acc;
+            }
+        }
+    }
+}
+
 /* ---- q8_1 ----------------------------------------------------------------- */
 
 /* bf16 x [m, K] with row stride ldx (elements) -> q8_1 rows, K/32 blocks of
@@ -403,4 +471,5 @@ int oracle_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, 
 }
 
 int oracle_block_bytes(void) { return Q2K_BYTES; }
+int oracle_q3k_block_bytes(void) { return Q3K_BYTES; }
 int oracle_q8_1_block_bytes(void) { return Q8_1_BYTES; }

@@ -433,3 +433,115 @@ def test_engram_hash_ranges_blocking_and_incremental_calls():
     with pytest.raises(ValueError):
         oracle.engram_hash(tm, np.zeros(4, np.int64), ids[:5], 0, **args)
     np.testing.assert_array_equal(oracle.layer_row_ids(out, 1), out[:, 1, :].reshape(-1))
+
+
+# ---- Q3_K (moe_v41/init.rs, `MoeV41::new`, names the Q3_K MMVQ kernels; the
+# block layout is GGUF's Q3_K, a reading: hmask[32] | qs[64] | scales[12] | d) ----
+
+def make_q3k_block(scales6, codes, d):
+    """Pack 16 six-bit scales (0..63, stored +32) and 256 codes (-4..3) the
+    way GGUF's Q3_K quantiser lays them out."""
+    b = np.zeros(110, dtype=np.uint8)
+    for j, s in enumerate(scales6):
+        s = int(s)
+        if j < 8:
+            b[96 + j] |= s & 15
+        else:
+            b[96 + j - 8] |= (s & 15) << 4
+        b[96 + 8 + j % 4] |= (s >> 4) << (2 * (j // 4))
+    for p, c in enumerate(codes):
+        L = int(c) + 4
+        if L > 3:
+            b[p % 32] |= 1 << (p // 32)
+        b[32 + 32 * (p // 128) + p % 32] |= (L & 3) << (2 * ((p % 128) // 32))
+    b[108:110] = np.array([d], dtype=np.float16).view(np.uint8)
+    return b
+
+
+def test_q3k_block_is_110_bytes():
+    assert oracle.q3k_block_bytes() == 32 + 64 + 12 + 2 == 110
+
+
+def test_q3k_with_every_high_bit_set_is_q2k_without_a_min():
+    rng = np.random.default_rng(31)
+    for _ in range(20):
+        qs = rng.integers(0, 256, 64, dtype=np.uint8)
+        nib = rng.integers(0, 16, 16)
+        d = float(np.float16(rng.uniform(-0.05, 0.05)))
+        q3 = make_q3k_block(32 + nib, np.zeros(256, int), d)
+        q3[0:32] = 0xFF
+        q3[32:96] = qs
+        q2 = make_block(nib, qs, d, 0.0)
+        np.testing.assert_array_equal(oracle.q3k_decode_block(q3), oracle.decode_block(q2))
+
+
+def test_q3k_with_every_high_bit_clear_is_q2k_with_min_four_d_times_scale():
+    # code - 4 with the high bit clear: d*s*q - 4*d*s = Q2_K with min nibble s, dmin = 4d
+    rng = np.random.default_rng(32)
+    for _ in range(20):
+        qs = rng.integers(0, 256, 64, dtype=np.uint8)
+        nib = rng.integers(0, 16, 16)
+        d = float(np.float16(2.0 ** rng.integers(-12, -4)))
+        q3 = make_q3k_block(32 + nib, np.zeros(256, int), d)
+        q3[0:32] = 0
+        q3[32:96] = qs
+        q2 = make_block(nib | (nib << 4), qs, d, 4 * d)
+        np.testing.assert_array_equal(oracle.q3k_decode_block(q3), oracle.decode_block(q2))
+
+
+def test_q3k_each_hmask_bit_moves_exactly_one_weight_by_four_steps():
+    rng = np.random.default_rng(33)
+    scales6 = rng.integers(0, 64, 16)
+    codes = rng.integers(-4, 4, 256)
+    d = 0.0078125
+    base = make_q3k_block(scales6, codes, d)
+    w0 = oracle.q3k_decode_block(base)
+    hit = np.zeros(256, dtype=int)
+    for byte in range(32):
+        for bit in range(8):
+            blk = base.copy()
+            blk[byte] ^= 1 << bit
+            diff = oracle.q3k_decode_block(blk) - w0
+            (idx,) = np.nonzero(diff)
+            step = d * (int(scales6[idx[0] // 16]) - 32) if len(idx) else None
+            if scales6[(32 * bit + byte) // 16] == 32:  # a zero scale hides the change
+                assert len(idx) == 0
+                hit[32 * bit + byte] += 1
+                continue
+            assert list(idx) == [32 * bit + byte]
+            was_set = (base[byte] >> bit) & 1
+            assert diff[idx[0]] == (-4 if was_set else 4) * step
+            hit[idx[0]] += 1
+    assert (hit == 1).all()
+
+
+def test_q3k_six_bit_scales_round_trip_with_every_value():
+    # all 64 stored values over four blocks, each sub-block's weights = d*(s-32)
+    perm = np.random.default_rng(34).permutation(64)
+    d = 0.25
+    for blk_i in range(4):
+        s6 = perm[16 * blk_i:16 * blk_i + 16]
+        w = oracle.q3k_decode_block(make_q3k_block(s6, np.ones(256, int), d))
+        for j in range(16):
+            assert (w[16 * j:16 * j + 16] == d * (int(s6[j]) - 32)).all()
+
+
+def test_q3k_extremes_of_scale_and_code():
+    d = 0.5
+    w = oracle.q3k_decode_block(make_q3k_block([0] * 8 + [63] * 8, [-4] * 128 + [3] * 128, d))
+    assert (w[:128] == d * 128).all()  # (-32) * (-4)
+    assert (w[128:] == d * 93).all()   # 31 * 3
+
+
+@pytest.mark.parametrize("N,K,m", [(1, 256, 1), (3, 512, 2), (5, 256, 8), (4, 768, 3)])
+def test_q3k_matvec_equals_numpy_matmul_of_decoded_matrix(N, K, m):
+    rng = np.random.default_rng(N * 100 + K + m)
+    W = rng.integers(0, 256, N * (K // 256) * 110, dtype=np.uint8).reshape(N, -1)
+    for n in range(N):
+        for b in range(K // 256):
+            W[n, b * 110 + 108:b * 110 + 110] = np.array([rng.uniform(-0.02, 0.02)], np.float16).view(np.uint8)
+    x = rng.standard_normal((m, K))
+    Wd = oracle.q3k_decode_matrix(W, N, K)
+    np.testing.assert_allclose(oracle.q3k_matvec(W, N, K, x), x @ Wd.T, rtol=1e-12, atol=1e-12)
+    # block b of row n decodes on its own
+    np.testing.assert_array_equal(Wd[N - 1, K - 256:], oracle.q3k_decode_block(W[N - 1, -110:]))
