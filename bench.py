@@ -439,6 +439,52 @@ def sweep(q, L, l2, hbm, rank):
         rec(f"grouped wo_a MMVQ {G}x[{Rg},{Kg}] m={m}", el / n, Wg.nbytes + xq.numel() + 4 * m * G * Rg, m)
     del Wgs
 
+    # Q3_K twins (moe_v41/init.rs names them beside the Q2_K kernels): one matrix, and the
+    # experts batches at the MoE shapes (64 experts resident, selection varies per call)
+    for N, ms in ((4096, (1, 8)), (16384, (1, 2, 4, 8))):
+        K = N
+        W3 = synth.q3k_matrix(0, f"sweep.q3.W{N}", N, K)
+        R = copies_for(W3.nbytes, l2)
+        W30 = torch.from_numpy(W3).cuda()
+        W3s = [W30] + [W30.clone() for _ in range(R - 1)]
+        for m in ms:
+            xq = q.q8_1_quantize_rows(torch.from_numpy(synth.bf16_normal(0, f"sweep.q3.x{m}", (m, K)).view(np.int16))
+                                      .cuda().view(torch.bfloat16))
+            y = torch.empty((m, N), dtype=torch.float32, device="cuda")
+            el, n = graph_time(lambda i: check(L.q3k_mmvq_q8_1(P(W3s[i % R]), N, K, P(xq), m, P(y), N, cur()),
+                                               "q3k"), 2000, 100)
+            rec(f"q3k mmvq_q8_1 N={N} K={K} m={m}", el / n, W3.nbytes + xq.numel() + 4 * m * N, m)
+        del W3s, W30
+        torch.cuda.empty_cache()
+    E_pool, topk, dim, inter = 64, 8, 4096, 2048
+    q3 = {}
+    for e in range(E_pool):
+        for kind, shape in (("gate", (inter, dim)), ("up", (inter, dim)), ("down", (dim, inter))):
+            q3[(kind, e)] = torch.from_numpy(synth.q3k_matrix(0, f"q3moe.{kind}{e}", *shape)).cuda()
+    rng = np.random.default_rng(1)
+    gu_t, dn_t = [], []
+    for _ in range(32):
+        sel = [int(e) for e in rng.choice(E_pool, topk, replace=False)]
+        gu_t.append(q.pointer_table([q3[("gate", e)] for e in sel] + [q3[("up", e)] for e in sel]))
+        dn_t.append(q.pointer_table([q3[("down", e)] for e in sel]))
+    xq = q.q8_1_quantize_rows(torch.from_numpy(synth.bf16_normal(0, "q3moe.x", (1, dim)).view(np.int16))
+                              .cuda().view(torch.bfloat16))
+    hq = q.q8_1_quantize_rows(torch.from_numpy(synth.bf16_normal(0, "q3moe.h", (topk, inter)).view(np.int16))
+                              .cuda().view(torch.bfloat16))
+    y_gu = torch.empty((2 * topk, inter), dtype=torch.float32, device="cuda")
+    y_dn = torch.empty((topk, dim), dtype=torch.float32, device="cuda")
+    ys = torch.empty(dim, dtype=torch.float32, device="cuda")
+    wd = torch.from_numpy(synth.expert_route(0, 256, topk)[1]).cuda()
+    mb = inter * (dim // 256) * 110
+    el, n = graph_time(lambda i: check(L.q3k_mmvq_experts(P(gu_t[i % 32]), 2 * topk, inter, dim, P(xq), 0, P(y_gu),
+                                                          None, None, cur()), "q3k_ex"), 1000, 50)
+    rec("q3k experts gate/up batch 16x[2048,4096] m=1", el / n, 2 * topk * mb, 1)
+    el, n = graph_time(lambda i: check(L.q3k_mmvq_experts(P(dn_t[i % 32]), topk, dim, inter, P(hq), 1, P(y_dn),
+                                                          P(wd), P(ys), cur()), "q3k_ex"), 1000, 50)
+    rec("q3k experts down batch 8x[4096,2048] + weighted sum", el / n, topk * mb, 1, {"launches_per_call": 2})
+    del q3, gu_t, dn_t
+    torch.cuda.empty_cache()
+
     # cfg3: routed experts for one token (256 experts resident, selection varies per call)
     E_all, topk, dim, inter = 256, 8, 4096, 2048
     mats = {}

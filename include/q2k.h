@@ -73,6 +73,9 @@ enum q2k_status {
 /* Bytes of one Q2_K row of K weights: K/256*84, or 0 when K % 256 != 0. */
 size_t q2k_row_bytes(int64_t K);
 
+/* Bytes of one Q3_K row of K weights: K/256*110, or 0 when K % 256 != 0. */
+size_t q3k_row_bytes(int64_t K);
+
 /* Bytes of one q8_1 row of K values: K/32*36, or 0 when K % 32 != 0
  * (moe_v41/init.rs, `kquant_q8_1_rows_bytes`). */
 size_t q8_1_row_bytes(int64_t K);
@@ -209,6 +212,40 @@ int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64
                      const void* xq, int x_per_matrix, float* y, const float* route_w,
                      float* y_sum, q2k_stream_t stream);
 
+/* Q3_K twins (moe_v41/init.rs, `MoeV41::new`, loads `kquant_mmvq_q3_k_w`
+ * and `kquant_mmvq_q3_k_experts_w*` beside the Q2_K kernels; the pages give
+ * no Q3_K layout, so the block is GGUF's Q3_K, 110 bytes per 256 weights:
+ * hmask[32] | qs[64] | scales[12] | d (fp16 LE).  Weight p of a block is
+ * d * s_j * (code_p - 4 * (1 - high_p)), with j = p/16, s_j the signed
+ * 6-bit sub-block scale (stored + 32: low nibble in scales[j] for j < 8 or
+ * the high nibble of scales[j-8], top two bits at bit 2*(j/4) of
+ * scales[8 + j%4]), code_p the 2-bit field at bit 2*((p%128)/32) of
+ * qs[32*(p/128) + p%32] and high_p bit p/32 of hmask[p%32]).
+ *
+ * Single matrix, m = 1..8 tokens:
+ *   W    Q3_K [N, K], row-major blocks, 4-byte aligned
+ *   xq   m q8_1 rows of K values, back to back, 4-byte aligned
+ *   y    fp32, y[t*ldy + n] = sum_k W[n, k] * x_t[k], ldy >= N
+ * Errors before any launch: NULL_ARG, BAD_SHAPE (K % 256, K > 2^20, N < 1,
+ * m outside 1..8, ldy < N), MISALIGNED.  The sum is deterministic: the same
+ * inputs give the same bits on every call. */
+int q3k_mmvq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y, int64_t ldy,
+                  q2k_stream_t stream);
+
+/* Batched single-token Q3_K MMVQ over n_mat matrices of one shape.
+ *   W_table   device array of n_mat device pointers, each Q3_K [N, K]; an
+ *             entry that is not 4-byte aligned is skipped (its rows of y
+ *             are left as they were) and sets bit 1 of the device error word
+ *   xq        q8_1 input: one row shared by every matrix (x_per_matrix ==
+ *             0) or row e for matrix e (x_per_matrix == 1)
+ *   y         fp32 [n_mat, N], required; row e equals
+ *             q3k_mmvq_q8_1(W_table[e], its input row) bit for bit
+ *   route_w   fp32 [n_mat], required with y_sum
+ *   y_sum     fp32 [N], nullable: sum_e route_w[e]*y[e, n] in e order, a
+ *             second launch over y */
+int q3k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K, const void* xq,
+                     int x_per_matrix, float* y, const float* route_w, float* y_sum, q2k_stream_t stream);
+
 /* SwiGLU fused with q8_1 requantisation (moe_v41/init.rs,
  * `kquant_swiglu_q8_1_rows_bf16`).
  *   gate_up  fp32 [2E, N]: gate rows 0..E-1, up rows E..2E-1 (the layout
@@ -282,7 +319,8 @@ int q2k_last_cuda_error(void);
 /* Diagnostics, synchronous (not for use inside stream capture): reads the
  * device's library error word into *host_out (0 = none; bit 0 = a bounded
  * wait in a kernel gave up and that kernel returned early, outputs
- * incomplete) and clears it when clear != 0. */
+ * incomplete; bit 1 = a Q3_K table entry off a 4-byte boundary was
+ * skipped) and clears it when clear != 0. */
 int q2k_device_error(int32_t* host_out, int clear);
 
 #ifdef __cplusplus

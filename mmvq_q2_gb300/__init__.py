@@ -25,6 +25,7 @@ EXPORTS = (
     "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q2k_engram_hash", "q8_1_quantize_rows",
     "q2k_gemv_bf16",
     "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_grouped", "q2k_mmvq_experts",
+    "q3k_row_bytes", "q3k_mmvq_q8_1", "q3k_mmvq_experts",
     "swiglu_q8_1_rows",
     "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
     "q2k_last_cuda_error", "q2k_device_error",
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
             "q2k_mmvq_pair_bf16": (I32, [P, I64, P, P, I64, P, I64, P, I64, P, P]),
             "q2k_mmvq_grouped": (I32, [P, I64, I64, I64, P, I64, P, P]),
             "q2k_mmvq_experts": (I32, [P, I64, I64, I64, P, I32, P, P, P, P]),
+            "q3k_row_bytes": (SZ, [I64]),
+            "q3k_mmvq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P]),
+            "q3k_mmvq_experts": (I32, [P, I64, I64, I64, P, I32, P, P, P, P]),
             "swiglu_q8_1_rows": (I32, [P, I64, I64, P, P, P]),
             "q2k_moe_m1_workspace_bytes": (SZ, [I64, I64, I64]),
             "q2k_moe_m1": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
@@ -241,6 +245,34 @@ def q2k_mmvq_experts(W_table, N, K, xq, x_per_matrix=False, y=None, route_w=None
     if y is None and want_y:
         y = torch.empty((n_mat, N), dtype=torch.float32, device=xq.device)
     _call("q2k_mmvq_experts", _ptr(W_table), n_mat, N, K, _ptr(xq), 1 if x_per_matrix else 0, _ptr(y),
+          _ptr(route_w), _ptr(y_sum), _stream(stream))
+    return y, y_sum
+
+
+def q3k_row_bytes(K) -> int:
+    return lib().q3k_row_bytes(K)
+
+
+def q3k_mmvq_q8_1(W, xq, K, out=None, stream=None):
+    """Q3_K ``[N, K]`` (110-byte GGUF blocks) times q8_1 ``xq [m, K/32*36]``
+    -> fp32 ``[m, N]``."""
+    _need_cuda(W, xq, out)
+    m = xq.shape[0]
+    N = W.numel() // q3k_row_bytes(K)
+    if out is None:
+        out = torch.empty((m, N), dtype=torch.float32, device=xq.device)
+    _call("q3k_mmvq_q8_1", _ptr(W), N, K, _ptr(xq), m, _ptr(out), out.stride(0), _stream(stream))
+    return out
+
+
+def q3k_mmvq_experts(W_table, N, K, xq, x_per_matrix=False, y=None, route_w=None, y_sum=None, stream=None):
+    """Batched single-token Q3_K MMVQ over the matrices in ``W_table``;
+    optional route-weighted ``y_sum`` -> (y, y_sum)."""
+    _need_cuda(W_table, xq, y, route_w, y_sum)
+    n_mat = W_table.numel()
+    if y is None:
+        y = torch.empty((n_mat, N), dtype=torch.float32, device=xq.device)
+    _call("q3k_mmvq_experts", _ptr(W_table), n_mat, N, K, _ptr(xq), 1 if x_per_matrix else 0, _ptr(y),
           _ptr(route_w), _ptr(y_sum), _stream(stream))
     return y, y_sum
 

@@ -92,6 +92,13 @@ size_t q2k_row_bytes(int64_t K)
     return (size_t)(K / kBlockWeights) * kBlockBytes;
 }
 
+size_t q3k_row_bytes(int64_t K)
+{
+    if (K <= 0 || K % kBlockWeights)
+        return 0;
+    return (size_t)(K / kBlockWeights) * 110;
+}
+
 size_t q8_1_row_bytes(int64_t K)
 {
     if (K <= 0 || K % kQ8Values)
@@ -119,7 +126,7 @@ int q2k_device_error(int32_t* host_out, int clear)
 {
     if (!host_out)
         return Q2K_ERR_NULL_ARG;
-    int32_t a = 0, b = 0, c = 0, d = 0;
+    int32_t a = 0, b = 0, c = 0, d = 0, q = 0;
     cudaError_t e = mv_error_word(&a, clear != 0);
     if (e == cudaSuccess)
         e = gemm_error_word(&b, clear != 0);
@@ -127,9 +134,11 @@ int q2k_device_error(int32_t* host_out, int clear)
         e = mt_error_word(&c, clear != 0);
     if (e == cudaSuccess)
         e = umma_error_word(&d, clear != 0);
+    if (e == cudaSuccess)
+        e = q3_error_word(&q, clear != 0);
     if (e != cudaSuccess)
         return fail_cuda(e);
-    *host_out = a | b | c | d;
+    *host_out = a | b | c | d | q;
     return Q2K_OK;
 }
 
@@ -391,6 +400,64 @@ int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64
         return finish(launch_expert_sum(y, route_w, n_mat, N, y_sum, s));
     }
     return finish(launch_mv(p, s));
+}
+
+int q3k_mmvq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y, int64_t ldy,
+                  q2k_stream_t stream)
+{
+    if (!W || !xq || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (N <= 0 || N > (1 << 30) || K <= 0 || K % kBlockWeights || K > kMaxK || m < 1 || m > 8 || ldy < N)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W, 4) || !aligned(xq, 4) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    Q3Problem p{};
+    p.W = W;
+    p.n_seg = 1;
+    p.N = N;
+    p.K = K;
+    p.m = (int)m;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    p.y = y;
+    p.ldy = ldy;
+    return finish(launch_q3k_mv(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q3k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K, const void* xq,
+                     int x_per_matrix, float* y, const float* route_w, float* y_sum, q2k_stream_t stream)
+{
+    if (!W_table || !xq || !y || (y_sum && !route_w))
+        return Q2K_ERR_NULL_ARG;
+    if (n_mat <= 0 || n_mat > 4096 || N <= 0 || N > (1 << 30) || K <= 0 || K % kBlockWeights || K > kMaxK ||
+        (x_per_matrix != 0 && x_per_matrix != 1))
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W_table, 8) || !aligned(xq, 4) || !aligned(y, 4) || (route_w && !aligned(route_w, 4)) ||
+        (y_sum && !aligned(y_sum, 4)))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    Q3Problem p{};
+    p.W_table = W_table;
+    p.n_seg = (int)n_mat;
+    p.N = N;
+    p.K = K;
+    p.m = 1;
+    p.x = xq;
+    p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
+    p.x_seg_stride = x_per_matrix ? (int64_t)q8_1_row_bytes(K) : 0;
+    p.y = y;
+    p.ldy = N;
+    p.y_seg_stride = N;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_q3k_mv(p, s);
+    if (e != cudaSuccess || !y_sum)
+        return e != cudaSuccess ? fail_cuda(e) : finish(e);
+    return finish(launch_expert_sum(y, route_w, n_mat, N, y_sum, s));
 }
 
 int swiglu_q8_1_rows(const float* gate_up, int64_t E, int64_t N, void* h_q8, uint16_t* h_bf16, q2k_stream_t stream)

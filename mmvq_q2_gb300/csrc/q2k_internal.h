@@ -78,10 +78,28 @@ bool umma_supported(int64_t m, int64_t K, int64_t N);
 cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
                                  int64_t N, float* y, int64_t ldy, cudaStream_t s);
 
+// Q3_K MMVQ with q8_1 activations (m = 1..8): one matrix, or n_seg matrices
+// from W_table (N rows each, y row block e at y + e * y_seg_stride).
+struct Q3Problem {
+    const void* W;
+    const void* const* W_table;
+    int n_seg;
+    int64_t N, K;
+    int m;
+    const void* x;
+    int64_t x_tok_stride;  // bytes between tokens
+    int64_t x_seg_stride;  // bytes between segments' inputs (0 = shared)
+    float* y;
+    int64_t ldy;           // floats between tokens
+    int64_t y_seg_stride;  // floats between segments
+};
+cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s);
+
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
 cudaError_t gemm_error_word(int32_t* out, bool clear);
 cudaError_t mt_error_word(int32_t* out, bool clear);
 cudaError_t umma_error_word(int32_t* out, bool clear);
+cudaError_t q3_error_word(int32_t* out, bool clear);
 
 }  // namespace q2k

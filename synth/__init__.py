@@ -12,6 +12,10 @@ Recipe (the workloads of the engram / attention / MoE decode pages):
   uniform u8, ``d`` and ``dmin`` uniform in [1e-3, 1e-2] drawn in fp32 and
   rounded to fp16 (round to nearest even).  Block layout
   ``scales[16] | qs[64] | d (fp16 LE) | dmin (fp16 LE)`` = 84 bytes.
+* Q3_K bytes (GGUF layout ``hmask[32] | qs[64] | scales[12] | d``, 110
+  bytes): the first 108 bytes uniform u8 (so every 6-bit scale and every
+  3-bit code is uniform), ``d`` of either sign with magnitude uniform in
+  [1e-3, 1e-2], rounded to fp16.
 * Activations: bf16 from N(0, 1) (fp32 draw, round to nearest even).
 * Dense bf16 weights: N(0, 0.02).
 * Engram row ids: uniform integers in [0, n_table_rows), with replacement.
@@ -26,6 +30,7 @@ import numpy as np
 
 Q2K_BLOCK_BYTES = 84
 Q2K_BLOCK_WEIGHTS = 256
+Q3K_BLOCK_BYTES = 110
 
 
 def rng(seed: int, name: str) -> np.random.Generator:
@@ -66,6 +71,19 @@ def q2k_matrix(seed: int, name: str, n_rows: int, k: int) -> np.ndarray:
         raise ValueError(f"K={k} is not a multiple of 256")
     nb = k // Q2K_BLOCK_WEIGHTS
     return q2k_blocks(seed, name, n_rows * nb).reshape(n_rows, nb * Q2K_BLOCK_BYTES)
+
+
+def q3k_matrix(seed: int, name: str, n_rows: int, k: int) -> np.ndarray:
+    """A row-major ``[n_rows, k]`` Q3_K weight as ``[n_rows, k/256*110]`` bytes."""
+    if k % Q2K_BLOCK_WEIGHTS:
+        raise ValueError(f"K={k} is not a multiple of 256")
+    n_blocks = n_rows * (k // Q2K_BLOCK_WEIGHTS)
+    g = rng(seed, name)
+    out = np.empty((n_blocks, Q3K_BLOCK_BYTES), dtype=np.uint8)
+    out[:, 0:108] = g.integers(0, 256, size=(n_blocks, 108), dtype=np.uint8)
+    d = g.uniform(1e-3, 1e-2, size=n_blocks) * np.where(g.integers(0, 2, size=n_blocks) == 1, 1.0, -1.0)
+    out[:, 108:110] = d.astype(np.float32).astype(np.float16).view(np.uint8).reshape(n_blocks, 2)
+    return out.reshape(n_rows, -1)
 
 
 def bf16_normal(seed: int, name: str, shape, std: float = 1.0) -> np.ndarray:

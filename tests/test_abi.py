@@ -114,6 +114,27 @@ def test_mmvq_pair_experts_validation(L):
     assert L.q2k_mmvq_experts(P(0x10004), 8, 64, 512, FAKE, 0, FAKE, None, None, None) == 3
 
 
+
+def test_q3k_validation(L):
+    assert L.q3k_row_bytes(256) == 110 and L.q3k_row_bytes(4096) == 16 * 110 and L.q3k_row_bytes(100) == 0
+    # single matrix: K multiple of 256, m in 1..8, ldy >= N, 4-byte alignment
+    assert L.q3k_mmvq_q8_1(None, 4, 512, FAKE, 1, FAKE, 4, None) == 1
+    assert L.q3k_mmvq_q8_1(FAKE, 4, 500, FAKE, 1, FAKE, 4, None) == 2
+    assert L.q3k_mmvq_q8_1(FAKE, 4, 512, FAKE, 0, FAKE, 4, None) == 2
+    assert L.q3k_mmvq_q8_1(FAKE, 4, 512, FAKE, 9, FAKE, 4, None) == 2
+    assert L.q3k_mmvq_q8_1(FAKE, 4, 512, FAKE, 1, FAKE, 3, None) == 2
+    assert L.q3k_mmvq_q8_1(FAKE, 0, 512, FAKE, 1, FAKE, 4, None) == 2
+    assert L.q3k_mmvq_q8_1(P(0x10002), 4, 512, FAKE, 1, FAKE, 4, None) == 3
+    assert L.q3k_mmvq_q8_1(FAKE, 4, 512, P(0x10002), 1, FAKE, 4, None) == 3
+    # experts: y required, y_sum needs route weights, x_per_matrix 0 or 1
+    assert L.q3k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, None, None, None, None) == 1
+    assert L.q3k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 0, FAKE, None, FAKE, None) == 1
+    assert L.q3k_mmvq_experts(FAKE, 8, 64, 512, FAKE, 2, FAKE, None, None, None) == 2
+    assert L.q3k_mmvq_experts(FAKE, 0, 64, 512, FAKE, 0, FAKE, None, None, None) == 2
+    assert L.q3k_mmvq_experts(FAKE, 8, 64, 768 + 1, FAKE, 0, FAKE, None, None, None) == 2
+    assert L.q3k_mmvq_experts(P(0x10004), 8, 64, 512, FAKE, 0, FAKE, None, None, None) == 3
+
+
 def test_small_kernels_validation(L):
     assert L.q2k_dequant_rows(None, 4, 256, None, 1, FAKE, None, None) == 1
     assert L.q2k_dequant_rows(FAKE, 4, 200, None, 1, FAKE, None, None) == 2
