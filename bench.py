@@ -17,7 +17,7 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   and x from pinned host memory, calls the C ABI, and reads y back.
 * cpu_baseline times the CPU oracle (one thread) on a bounded sample.
 * --impl reference times the CPU oracle on the same workload (rank 0 only).
-* --ncu-case [mv|mt|gemm|small] runs a few untimed calls for a profiler
+* --ncu-case [mv|mt|gemm|small|q3k] runs a few untimed calls for a profiler
   capture and prints no JSON line: mv = the headline kernel (bf16 GEMV) and
   the q8_1 MMVQ at m=1 on the headline shape; mt = the same shape at m=8
   (the tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
@@ -654,13 +654,26 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     between passes; one weight copy).  mv: `calls` eager calls of
     q2k_gemv_bf16, then of q2k_mmvq_q8_1, at m=1 N=K=16384 (88 MB of
     weights).  mt: the same at m=8.  gemm: dense_gemm_bf16 at m=64, then
-    m=256, N=K=16384 (537 MB of bf16 weights), one call each."""
+    m=256, N=K=16384 (537 MB of bf16 weights), one call each.  q3k:
+    `calls` calls of q3k_mmvq_q8_1 at m=1, then at m=2, N=K=16384 (115 MB of
+    Q3_K weights)."""
     import torch
     from mmvq_q2_gb300 import build as b
     b.build()
     import mmvq_q2_gb300 as q
     if which == "small":
         _ncu_small_case(q)
+        torch.cuda.synchronize()
+        print("ncu case done", file=sys.stderr)
+        return
+    if which == "q3k":
+        W = synth.q3k_matrix(0, "sweep.q3.W16384", N_HEAD, K_HEAD)
+        Wd = torch.from_numpy(W).cuda()
+        for m in (1, 2):
+            x = synth.bf16_normal(0, f"sweep.q3.x{m}", (m, K_HEAD))
+            xq = q.q8_1_quantize_rows(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+            for _ in range(calls):
+                q.q3k_mmvq_q8_1(Wd, xq, K_HEAD)
         torch.cuda.synchronize()
         print("ncu case done", file=sys.stderr)
         return
@@ -693,7 +706,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
-    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small"], default=None)
+    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
         run_ncu_case(args.ncu_case)

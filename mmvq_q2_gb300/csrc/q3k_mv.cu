@@ -13,21 +13,35 @@
 // Design (GB300):
 //  * Each lane owns a fixed K-slice: LW consecutive byte positions l of one
 //    block column, i.e. 8*LW weights (every n and j).  The q8_1 activations
-//    of that slice stay in registers for every row the lane visits, so the
-//    per-row traffic is the weight stream alone.
+//    of that slice (for MG tokens at a time) stay in registers for every row
+//    the lane visits, so the per-row traffic is the weight stream alone.
+//  * A warp owns one chunk of LW block columns.  It copies each row's chunk
+//    (LW*110 bytes, contiguous) into its own shared-memory buffer with
+//    coalesced 16-byte loads (4-byte loads when rows are not 16-byte
+//    aligned), issued one row ahead so they overlap the arithmetic; the
+//    lanes then read their fields from shared memory.  Read straight from
+//    global memory, each lane's scattered 32-bit reads cost an L1 wavefront
+//    per sector.  What bounds the kernel now is the same unit: the lanes'
+//    word reads of 16 blocks 110 bytes apart meet in the same banks (about
+//    3.6 wavefronts per read), with issue about two thirds busy.
+//    Only __syncwarp orders the buffer: no waits between warps or CTAs.
 //  * Blocks are 110 bytes, so every other block starts 2 bytes off a word:
-//    each field is read with aligned 32-bit loads and a funnel shift.  No
-//    staging and no waits: nothing in this kernel can stall on another CTA.
-//  * Per (n, j), with c = 4n + j: the codes stay at bit 2j (one AND a word;
-//    the 4^j comes off the int32 sum with a shift), the complement of the
-//    high bit at bit c (one AND-NOT a word); two DP4A a word give
-//    S1 = 4^j * sum(code*q) and S2 = 2^c * sum((1-high)*q), and
-//    sum((code + 4*high - 4)*q) = S1 / 4^j - 4 * S2 / 2^c exactly.  The
-//    sub-block scale multiplies in int32, the q8_1 scale in fp32.
-//  * A warp's lanes cover one chunk of LW block columns; a butterfly
-//    shuffle sum gives every lane the chunk's partial for a row, kept in
-//    shared memory; after one barrier the chunks are added in chunk order,
-//    so the result does not depend on scheduling.
+//    fields are read as aligned words and funnel-shifted.
+//  * Per (n, j), with c = 4n + j: the code stays at bit 2j of each byte
+//    (one AND a word) and the high bit is shifted to bit 2j + 2 beside it
+//    (one shift and one AND-OR), so a single DP4A a word multiplies
+//    4^j * (code + 4*high) (16 * (...) for j = 3, from bit 4); the chain
+//    starts at -4 * 4^j * sum(q) of the slice (activations only, made once)
+//    and a shift takes the 4^j off exactly: one DP4A per four weights and
+//    token, half of what separate code and high-bit products need.  The
+//    sub-block scale multiplies in int32 and the product becomes fp32
+//    through the 1.5*2^23 bias (one IMAD and one FADD, exact below 2^22),
+//    then meets the q8_1 scale in one FFMA.
+//  * Several tokens run in groups of two inside the launch; each group
+//    walks the warp's rows again (the second pass reads L2).
+//  * A butterfly shuffle sum gives every lane the chunk's partial for a
+//    row, kept in shared memory; after one barrier the chunks are added in
+//    chunk order, so the result does not depend on scheduling.
 #include "q2k_common.cuh"
 #include "q2k_internal.h"
 
@@ -53,22 +67,29 @@ struct Q3Args {
     int64_t ldy;           // floats between tokens
     int64_t y_seg_stride;  // floats between segments
     int N, nb, nch, rows_per_cta;
+    int m;      // tokens (groups of MG walk the rows in turn)
+    int vec16;  // rows are 16-byte multiples: chunks move in 16-byte pieces
 };
+
+// Bytes of a warp's staging buffer for slice width lw: one row's chunk of
+// lw blocks plus the 2-byte lead of an unaligned copy, in 16-byte units.
+__host__ __device__ constexpr int q3_buf_bytes(int lw) { return ((lw * 110 + 4 + 15) / 16) * 16; }
 
 __device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) { return __ldg(reinterpret_cast<const unsigned int*>(p)); }
 
-// NW words from a 2-byte aligned address p: aligned loads of NW + 1 words
-// and a funnel shift by 0 or 16 bits.  Bytes read: [p - 2, p + 4*NW + 4).
+// NW words from a 2-byte aligned shared-memory address p: aligned reads of
+// NW + 1 words and a funnel shift by 0 or 16 bits.  Bytes read: [p - 2,
+// p + 4*NW + 4), all inside the block that holds p for every field below.
 template <int NW>
-__device__ __forceinline__ void ldg_words_a2(const uint8_t* p, uint32_t (&out)[NW])
+__device__ __forceinline__ void lds_words_a2(const uint8_t* p, uint32_t (&out)[NW])
 {
     const uintptr_t u = reinterpret_cast<uintptr_t>(p);
-    const uint8_t* pa = reinterpret_cast<const uint8_t*>(u & ~uintptr_t(3));
+    const uint32_t* pa = reinterpret_cast<const uint32_t*>(u & ~uintptr_t(3));
     const uint32_t sh = (uint32_t)(u & 2) * 8;
     uint32_t w[NW + 1];
 #pragma unroll
     for (int i = 0; i <= NW; ++i)
-        w[i] = ldg_u32(pa + 4 * i);
+        w[i] = pa[i];
 #pragma unroll
     for (int i = 0; i < NW; ++i)
         out[i] = __funnelshift_r(w[i], w[i + 1], sh);
@@ -82,36 +103,36 @@ struct Q3Slice {
 };
 
 template <int WPL>
-__device__ __forceinline__ void load_slice(const uint8_t* blk, int l0, Q3Slice<WPL>& s)
+__device__ __forceinline__ void read_slice(const uint8_t* blk, int l0, Q3Slice<WPL>& s)
 {
-    ldg_words_a2<WPL>(blk + l0, s.hm);
-    ldg_words_a2<WPL>(blk + 32 + l0, s.q0);
-    ldg_words_a2<WPL>(blk + 64 + l0, s.q1);
+    lds_words_a2<WPL>(blk + l0, s.hm);
+    lds_words_a2<WPL>(blk + 32 + l0, s.q0);
+    lds_words_a2<WPL>(blk + 64 + l0, s.q1);
     // scales[12] at byte 96: the four aligned words from byte 92 (block on a
-    // word) or 94 (block 2 bytes off), shifted right by 4 or 2 bytes; every
-    // byte read lies inside the block
+    // word) or 94 (block 2 bytes off), shifted right by 4 or 2 bytes
     const uintptr_t u = reinterpret_cast<uintptr_t>(blk) + 94;
-    const uint8_t* pa = reinterpret_cast<const uint8_t*>(u & ~uintptr_t(3));
+    const uint32_t* pa = reinterpret_cast<const uint32_t*>(u & ~uintptr_t(3));
     const uint32_t sh = 16 + (uint32_t)(u & 2) * 8;
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        w[i] = ldg_u32(pa + 4 * i);
+        w[i] = pa[i];
 #pragma unroll
     for (int i = 0; i < 3; ++i)
         s.sc[i] = __funnelshift_rc(w[i], w[i + 1], sh);
-    s.d = __ldg(reinterpret_cast<const unsigned short*>(blk + 108));
+    s.d = *reinterpret_cast<const uint16_t*>(blk + 108);
 }
 
 // Partial dot products of one slice with MG tokens' activations.
 // xq[t][4n + j][w]: q8 bytes l0 + 4w.. of q8_1 block 4n + j of this block
-// column; d8[t][4n + j] its scale.
+// column; d8[t][4n + j] its scale; c4[t][4n + j] = -4 * (sum of those q8
+// bytes) * 4^j (16 for j = 3), the start of the (n, j) DP4A chain.
 template <int MG, int WPL>
 __device__ __forceinline__ void dot_slice(const Q3Slice<WPL>& s, uint32_t lsel, uint32_t hsel,
                                           const uint32_t (&xq)[MG][8][WPL], const float (&d8)[MG][8],
-                                          float (&out)[MG])
+                                          const int (&c4)[MG][8], float (&out)[MG])
 {
-    // 6-bit scales of sub-blocks 8n + 2j + hs as bytes j of s6[n]
+    // 6-bit scales of sub-blocks 8n + 2j + hs as bytes j of s6_n
     const uint32_t L = __byte_perm(s.sc[0], s.sc[1], lsel);
     const uint32_t H = __byte_perm(s.sc[2], 0u, hsel);
     const uint32_t s6_0 = (L & 0x0F0F0F0Fu) | (((H & 0x00000303u) | ((H >> 2) & 0x03030000u)) << 4);
@@ -126,22 +147,27 @@ __device__ __forceinline__ void dot_slice(const Q3Slice<WPL>& s, uint32_t lsel, 
         for (int j = 0; j < 4; ++j) {
             const int c = 4 * n + j;
             const int sc = (int)(((n ? s6_1 : s6_0) >> (8 * j)) & 0xFFu) - 32;
-            uint32_t a[WPL], h[WPL];
+            // code + 4*high at bits 2j.. of each byte (4j.. for j = 3: 16*(code + 4*high)),
+            // so one DP4A per word multiplies the whole 3-bit value
+            const int pos = j < 3 ? 2 * j + 2 : 6;  // where the high bit goes
+            uint32_t v[WPL];
 #pragma unroll
             for (int w = 0; w < WPL; ++w) {
-                a[w] = (n ? s.q1[w] : s.q0[w]) & (0x03030303u << (2 * j));
-                h[w] = ~s.hm[w] & (0x01010101u << c);
+                const uint32_t q = n ? s.q1[w] : s.q0[w];
+                const uint32_t lo = j < 3 ? (q & (0x03030303u << (2 * j))) : ((q >> 2) & 0x30303030u);
+                const uint32_t hi = c >= pos ? (s.hm[w] >> (c - pos)) : (s.hm[w] << (pos - c));
+                v[w] = lo | (hi & (0x01010101u << pos));
             }
 #pragma unroll
             for (int t = 0; t < MG; ++t) {
-                int s1 = 0, s2 = 0;
+                int s4 = c4[t][c];
 #pragma unroll
-                for (int w = 0; w < WPL; ++w) {
-                    s1 = dp4a_us(a[w], xq[t][c][w], s1);
-                    s2 = dp4a_us(h[w], xq[t][c][w], s2);
-                }
-                const int S = (s1 >> (2 * j)) - (c >= 2 ? (s2 >> (c - 2)) : s2 * (1 << (2 - c)));
-                acc[t] = fmaf(d8[t][c], (float)(sc * S), acc[t]);
+                for (int w = 0; w < WPL; ++w)
+                    s4 = dp4a_us(v[w], xq[t][c][w], s4);
+                const int S = s4 >> (j < 3 ? 2 * j : 4);  // exact: every term carries the factor
+                // |sc * S| <= 32 * 16*4*128 < 2^22: exact through the bias
+                const float f = __int_as_float(0x4B400000 + sc * S) - 12582912.0f;
+                acc[t] = fmaf(d8[t][c], f, acc[t]);
             }
         }
     }
@@ -161,13 +187,89 @@ __device__ __forceinline__ void warp_sum(float (&v)[MG])
             v[t] += __shfl_xor_sync(0xFFFFFFFFu, v[t], off);
 }
 
+// One row's chunk in flight: 16-byte pieces (vec16) or words plus a 2-byte
+// tail, held in registers between the global loads and the shared stores.
+template <int NV>
+struct Q3Stage {
+    uint32_t v[4 * NV];
+    uint32_t tail;
+};
+
+// Global loads of the chunk [src, src + span): with vec16, src and span are
+// 16-byte multiples; otherwise src is 2-byte aligned and the copy covers
+// [src & ~3, src + span) as words (the bytes below src belong to the
+// previous block of the matrix) and the last 2 bytes when src + span is 2
+// bytes off a word.  No byte at or past src + span is read.
+template <int NV>
+__device__ __forceinline__ void stage_load(const uint8_t* src, int span, bool vec16, int lane, Q3Stage<NV>& st)
+{
+    if (vec16) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int k = lane + 32 * i;
+            if (k * 16 < span) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(src) + k);
+                st.v[4 * i] = q.x;
+                st.v[4 * i + 1] = q.y;
+                st.v[4 * i + 2] = q.z;
+                st.v[4 * i + 3] = q.w;
+            }
+        }
+    } else {
+        const uintptr_t u = reinterpret_cast<uintptr_t>(src);
+        const uint32_t* pa = reinterpret_cast<const uint32_t*>(u & ~uintptr_t(3));
+        const int end = (int)(u & 2) + span;  // bytes from pa
+        const int nfull = end >> 2;
+#pragma unroll
+        for (int i = 0; i < 4 * NV; ++i) {
+            const int k = lane + 32 * i;
+            if (k < nfull)
+                st.v[i] = __ldg(pa + k);
+        }
+        if ((end & 2) && lane == 0)
+            st.tail = __ldg(reinterpret_cast<const unsigned short*>(pa + nfull));
+    }
+}
+
+// The matching shared stores: the chunk's first byte lands at
+// buf + (vec16 ? 0 : (src & 2)).
+template <int NV>
+__device__ __forceinline__ void stage_store(const uint8_t* src, int span, bool vec16, int lane, const Q3Stage<NV>& st,
+                                            uint8_t* buf)
+{
+    if (vec16) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int k = lane + 32 * i;
+            if (k * 16 < span)
+                reinterpret_cast<uint4*>(buf)[k] = make_uint4(st.v[4 * i], st.v[4 * i + 1], st.v[4 * i + 2],
+                                                              st.v[4 * i + 3]);
+        }
+    } else {
+        const int end = (int)(reinterpret_cast<uintptr_t>(src) & 2) + span;
+        const int nfull = end >> 2;
+#pragma unroll
+        for (int i = 0; i < 4 * NV; ++i) {
+            const int k = lane + 32 * i;
+            if (k < nfull)
+                reinterpret_cast<uint32_t*>(buf)[k] = st.v[i];
+        }
+        if ((end & 2) && lane == 0)
+            *reinterpret_cast<uint16_t*>(buf + 4 * nfull) = (uint16_t)st.tail;
+    }
+}
+
 template <int MG, int LW>
 __global__ void __launch_bounds__(kQ3Threads, 2) q3k_mv_kernel(const Q3Args a)
 {
-    constexpr int WPL = LW / 4;    // words per lane per field
-    constexpr int LPB = 32 / LW;   // lanes per block column
-    constexpr int BPC = 32 / LPB;  // block columns per chunk
-    extern __shared__ float part[];  // [rows_per_cta][nch][MG]
+    constexpr int WPL = LW / 4;               // words per lane per field
+    constexpr int LPB = 32 / LW;              // lanes per block column
+    constexpr int BPC = 32 / LPB;             // block columns per chunk
+    constexpr int SPAN = BPC * kQ3Bytes;      // bytes of one row's chunk
+    constexpr int NV = (SPAN + 511) / 512;    // 16-byte loads per lane
+    constexpr int BUF = q3_buf_bytes(LW);     // the warp's staging buffer
+    static_assert((SPAN + 2) / 4 <= 32 * 4 * NV, "the word path fits the stage registers");
+    extern __shared__ __align__(16) uint8_t q3_smem[];  // 8 buffers, then partials [rows][nch][m]
 
     pdl_launch_dependents();
     const int seg = blockIdx.y;
@@ -182,12 +284,15 @@ __global__ void __launch_bounds__(kQ3Threads, 2) q3k_mv_kernel(const Q3Args a)
             atomicOr(&g_q3_error, 2);
         return;
     }
+    const bool vec16 = a.vec16 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
     const uint8_t* x = a.x + (int64_t)seg * a.x_seg_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* buf = q3_smem + warp * BUF;
+    float* part = reinterpret_cast<float*>(q3_smem + 8 * BUF);
     const int bl = lane / LPB, l0 = (lane % LPB) * LW, hs = l0 >> 4;
     const uint32_t lsel = hs ? 0x7531u : 0x6420u;
     const uint32_t hsel = hs ? 0x3131u : 0x2020u;
-    const int nch = a.nch;
+    const int nch = a.nch, m = a.m;
     // nch < 8: chunk warp % nch, rows split over 8 / nch warps;
     // nch >= 8: chunks warp, warp + 8, ..., every row
     const int c_step = nch >= 8 ? 8 : nch;
@@ -195,72 +300,79 @@ __global__ void __launch_bounds__(kQ3Threads, 2) q3k_mv_kernel(const Q3Args a)
     const int rg = nch >= 8 ? 0 : warp / nch;
     const int64_t row_bytes = (int64_t)a.nb * kQ3Bytes;
 
-    if (warp < c_step * wpc) {
+    if (warp < c_step * wpc && rg < nrows) {
         for (int c = warp % c_step; c < nch; c += c_step) {
             const int b = c * BPC + bl;
             const bool valid = b < a.nb;
-            uint32_t xq[MG][8][WPL];
-            float d8[MG][8];
+            const int span = min(BPC, a.nb - c * BPC) * kQ3Bytes;
+            const uint8_t* src0 = W + (int64_t)r0 * row_bytes + (int64_t)c * SPAN;
+            for (int t0 = 0; t0 < m; t0 += MG) {
+                uint32_t xq[MG][8][WPL];
+                float d8[MG][8];
+                int c4[MG][8];
 #pragma unroll
-            for (int t = 0; t < MG; ++t)
+                for (int t = 0; t < MG; ++t) {
+                    const bool on = valid && t0 + t < m;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint8_t* xb = x + (int64_t)t * a.x_tok_stride + ((int64_t)b * 8 + k) * kQ8Bytes;
-                    d8[t][k] = valid ? half_lo_f(ldg_u32(xb)) : 0.f;
+                    for (int k = 0; k < 8; ++k) {
+                        const uint8_t* xb = x + (int64_t)(t0 + t) * a.x_tok_stride + ((int64_t)b * 8 + k) * kQ8Bytes;
+                        d8[t][k] = on ? half_lo_f(ldg_u32(xb)) : 0.f;
+                        int sq = 0;
 #pragma unroll
-                    for (int w = 0; w < WPL; ++w)
-                        xq[t][k][w] = valid ? ldg_u32(xb + 4 + l0 + 4 * w) : 0u;
-                }
-            const uint8_t* wb = W + (int64_t)r0 * row_bytes + (int64_t)b * kQ3Bytes;
-            int r = rg;
-            for (; r + wpc < nrows; r += 2 * wpc) {  // two rows at a time: loads in flight
-                float v0[MG], v1[MG];
-                if (valid) {
-                    Q3Slice<WPL> s0, s1;
-                    load_slice(wb + (int64_t)r * row_bytes, l0, s0);
-                    load_slice(wb + (int64_t)(r + wpc) * row_bytes, l0, s1);
-                    dot_slice<MG, WPL>(s0, lsel, hsel, xq, d8, v0);
-                    dot_slice<MG, WPL>(s1, lsel, hsel, xq, d8, v1);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < MG; ++t)
-                        v0[t] = v1[t] = 0.f;
-                }
-                warp_sum(v0);
-                warp_sum(v1);
-                if (lane == 0)
-#pragma unroll
-                    for (int t = 0; t < MG; ++t) {
-                        part[(r * nch + c) * MG + t] = v0[t];
-                        part[((r + wpc) * nch + c) * MG + t] = v1[t];
+                        for (int w = 0; w < WPL; ++w) {
+                            xq[t][k][w] = on ? ldg_u32(xb + 4 + l0 + 4 * w) : 0u;
+                            sq = dp4a_us(0x01010101u, xq[t][k][w], sq);
+                        }
+                        const int j = k & 3;
+                        c4[t][k] = -4 * sq * (j < 3 ? (1 << (2 * j)) : 16);
                     }
-            }
-            if (r < nrows) {
-                float v0[MG];
-                if (valid) {
-                    Q3Slice<WPL> s0;
-                    load_slice(wb + (int64_t)r * row_bytes, l0, s0);
-                    dot_slice<MG, WPL>(s0, lsel, hsel, xq, d8, v0);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < MG; ++t)
-                        v0[t] = 0.f;
                 }
-                warp_sum(v0);
-                if (lane == 0)
+                int r = rg;
+                {
+                    Q3Stage<NV> st;
+                    stage_load(src0 + (int64_t)r * row_bytes, span, vec16, lane, st);
+                    stage_store(src0 + (int64_t)r * row_bytes, span, vec16, lane, st, buf);
+                }
+                __syncwarp();
+                for (; r < nrows; r += wpc) {
+                    const int rn = r + wpc;
+                    const uint8_t* src = src0 + (int64_t)r * row_bytes;
+                    Q3Stage<NV> nx;
+                    if (rn < nrows)  // the next row's chunk is in flight during this row's arithmetic
+                        stage_load(src0 + (int64_t)rn * row_bytes, span, vec16, lane, nx);
+                    float v[MG];
+                    if (valid) {
+                        const uint8_t* blk = buf + (vec16 ? 0 : (int)(reinterpret_cast<uintptr_t>(src) & 2)) +
+                                             bl * kQ3Bytes;
+                        Q3Slice<WPL> sl;
+                        read_slice(blk, l0, sl);
+                        dot_slice<MG, WPL>(sl, lsel, hsel, xq, d8, c4, v);
+                    } else {
 #pragma unroll
-                    for (int t = 0; t < MG; ++t)
-                        part[(r * nch + c) * MG + t] = v0[t];
+                        for (int t = 0; t < MG; ++t)
+                            v[t] = 0.f;
+                    }
+                    warp_sum(v);
+                    if (lane == 0)
+#pragma unroll
+                        for (int t = 0; t < MG; ++t)
+                            if (t0 + t < m)
+                                part[(r * nch + c) * m + t0 + t] = v[t];
+                    __syncwarp();  // every lane is done with the buffer
+                    if (rn < nrows)
+                        stage_store(src0 + (int64_t)rn * row_bytes, span, vec16, lane, nx, buf);
+                    __syncwarp();  // the next row is in the buffer
+                }
             }
         }
     }
     __syncthreads();
     float* y = a.y + (int64_t)seg * a.y_seg_stride;
-    for (int i = threadIdx.x; i < nrows * MG; i += kQ3Threads) {
-        const int r = i / MG, t = i - (i / MG) * MG;
+    for (int i = threadIdx.x; i < nrows * m; i += kQ3Threads) {
+        const int r = i / m, t = i - (i / m) * m;
         float s = 0.f;
         for (int c = 0; c < nch; ++c)
-            s += part[(r * nch + c) * MG + t];
+            s += part[(r * nch + c) * m + t];
         y[(int64_t)t * a.ldy + r0 + r] = s;
     }
 }
@@ -271,13 +383,11 @@ cudaError_t launch_q3_tpl(const Q3Args& a, int n_seg, int ctas_x, size_t smem, c
     return launch_pdl(q3k_mv_kernel<MG, LW>, dim3((unsigned)ctas_x, (unsigned)n_seg), dim3(kQ3Threads), smem, s, a);
 }
 
-// Slice width in bytes of l: 16 for one token over rows of 16+ blocks, 8
-// for two tokens (registers), 4 otherwise; narrower when the row has fewer
-// block columns than a warp chunk.
+// Slice width in bytes of l: 16 for one token, 8 for a group of two
+// (registers); narrower when the row has fewer block columns than a chunk.
 int q3_lw(int mg, int nb)
 {
-    const int want = mg == 1 ? 16 : (mg == 2 ? 8 : 4);
-    int lw = want;
+    int lw = mg == 1 ? 16 : 8;
     while (lw > 4 && nb < lw)
         lw /= 2;
     return lw;
@@ -292,44 +402,40 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
     if (e != cudaSuccess)
         return e;
     const int nb = (int)(p.K / 256);
-    for (int t0 = 0; t0 < p.m; t0 += 4) {
-        const int mg = std::min(4, p.m - t0);
-        const int lw = q3_lw(mg, nb);
-        Q3Args a{};
-        a.W = static_cast<const uint8_t*>(p.W);
-        a.W_table = p.W_table;
-        a.x = static_cast<const uint8_t*>(p.x) + (int64_t)t0 * p.x_tok_stride;
-        a.y = p.y + (int64_t)t0 * p.ldy;
-        a.x_tok_stride = p.x_tok_stride;
-        a.x_seg_stride = p.x_seg_stride;
-        a.ldy = p.ldy;
-        a.y_seg_stride = p.y_seg_stride;
-        a.N = (int)p.N;
-        a.nb = nb;
-        a.nch = (nb + lw - 1) / lw;
-        // two CTAs per SM over all segments; shared memory for the chunk
-        // partials stays within the default 48 KB
-        const int64_t target = std::max<int64_t>(1, (2 * (int64_t)di.sm_count + p.n_seg - 1) / p.n_seg);
-        int64_t rows = std::max<int64_t>(1, (p.N + target - 1) / target);
-        const int64_t max_rows = std::max<int64_t>(1, 49152 / ((int64_t)a.nch * mg * 4));
-        rows = std::min(rows, max_rows);
-        a.rows_per_cta = (int)rows;
-        const int ctas_x = (int)((p.N + rows - 1) / rows);
-        const size_t smem = (size_t)rows * a.nch * mg * sizeof(float);
-        switch (mg * 100 + lw) {
-        case 116: e = launch_q3_tpl<1, 16>(a, p.n_seg, ctas_x, smem, s); break;
-        case 108: e = launch_q3_tpl<1, 8>(a, p.n_seg, ctas_x, smem, s); break;
-        case 104: e = launch_q3_tpl<1, 4>(a, p.n_seg, ctas_x, smem, s); break;
-        case 208: e = launch_q3_tpl<2, 8>(a, p.n_seg, ctas_x, smem, s); break;
-        case 204: e = launch_q3_tpl<2, 4>(a, p.n_seg, ctas_x, smem, s); break;
-        case 304: e = launch_q3_tpl<3, 4>(a, p.n_seg, ctas_x, smem, s); break;
-        case 404: e = launch_q3_tpl<4, 4>(a, p.n_seg, ctas_x, smem, s); break;
-        default: return cudaErrorInvalidConfiguration;
-        }
-        if (e != cudaSuccess)
-            return e;
+    const int mg = p.m == 1 ? 1 : 2;
+    const int lw = q3_lw(mg, nb);
+    Q3Args a{};
+    a.W = static_cast<const uint8_t*>(p.W);
+    a.W_table = p.W_table;
+    a.x = static_cast<const uint8_t*>(p.x);
+    a.y = p.y;
+    a.x_tok_stride = p.x_tok_stride;
+    a.x_seg_stride = p.x_seg_stride;
+    a.ldy = p.ldy;
+    a.y_seg_stride = p.y_seg_stride;
+    a.N = (int)p.N;
+    a.nb = nb;
+    a.nch = (nb + lw - 1) / lw;
+    a.m = p.m;
+    a.vec16 = nb % 8 == 0;  // row bytes a 16-byte multiple (the base is checked per matrix)
+    // two CTAs per SM over all segments; staging buffers and chunk partials
+    // stay within the default 48 KB of shared memory
+    const int64_t bufs = 8 * (int64_t)q3_buf_bytes(lw);
+    const int64_t target = std::max<int64_t>(1, (2 * (int64_t)di.sm_count + p.n_seg - 1) / p.n_seg);
+    int64_t rows = std::max<int64_t>(1, (p.N + target - 1) / target);
+    const int64_t max_rows = std::max<int64_t>(1, (49152 - bufs) / ((int64_t)a.nch * p.m * 4));
+    rows = std::min(rows, max_rows);
+    a.rows_per_cta = (int)rows;
+    const int ctas_x = (int)((p.N + rows - 1) / rows);
+    const size_t smem = (size_t)(bufs + rows * a.nch * p.m * (int64_t)sizeof(float));
+    switch (mg * 100 + lw) {
+    case 116: return launch_q3_tpl<1, 16>(a, p.n_seg, ctas_x, smem, s);
+    case 108: return launch_q3_tpl<1, 8>(a, p.n_seg, ctas_x, smem, s);
+    case 104: return launch_q3_tpl<1, 4>(a, p.n_seg, ctas_x, smem, s);
+    case 208: return launch_q3_tpl<2, 8>(a, p.n_seg, ctas_x, smem, s);
+    case 204: return launch_q3_tpl<2, 4>(a, p.n_seg, ctas_x, smem, s);
+    default: return cudaErrorInvalidConfiguration;
     }
-    return cudaSuccess;
 }
 
 cudaError_t q3_error_word(int32_t* out, bool clear)
