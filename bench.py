@@ -24,8 +24,7 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   N=K=16384; small = one call of every other kernel at the configurations'
   shapes.
 * --all also times every configuration of the sweep and prints one JSON
-  object per configuration to stderr (and to gpurun_out/bench_all.jsonl when
-  that folder exists).
+  object per configuration to stderr (and to the file --all-out names).
 With torchrun (N > 1) every rank runs an independent replica (the path is
 replicated, not sharded); value = all ranks' bytes / the slowest rank's time.
 """
@@ -49,8 +48,8 @@ if ROOT not in sys.path:
 
 import synth  # noqa: E402
 
-BASELINE = json.load(open(os.path.join(ROOT, "BASELINE.json")))
-METRIC = BASELINE["metric"]
+# the headline metric: weight-stream GB/s of the m=1 Q2_K GEMV at N=K=16384
+METRIC = "Q2_K GEMV weight GB/s at m=1 (fraction of ~8 TB/s HBM); µs per decode projection"
 N_HEAD = K_HEAD = 16384
 W_BYTES_HEAD = N_HEAD * (K_HEAD // 256) * 84
 ALG_BYTES_HEAD = W_BYTES_HEAD + 2 * K_HEAD + 4 * N_HEAD  # weights + bf16 x + fp32 y
@@ -327,7 +326,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
         }
     if args.all:
-        sweep(q, L, l2, hbm, rank)
+        sweep(q, L, l2, hbm, rank, args.all_out)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -353,7 +352,7 @@ def cpu_baseline(W, x, budget_s: float = 20.0):
 
 # ---- sweep over every configuration (--all) ------------------------------------------------
 
-def sweep(q, L, l2, hbm, rank):
+def sweep(q, L, l2, hbm, rank, all_out=None):
     import torch
     out = []
 
@@ -566,8 +565,8 @@ def sweep(q, L, l2, hbm, rank):
         del Wds
         torch.cuda.empty_cache()
 
-    if rank == 0 and os.path.isdir(os.path.join(ROOT, "gpurun_out")):
-        with open(os.path.join(ROOT, "gpurun_out", "bench_all.jsonl"), "w") as f:
+    if rank == 0 and all_out:
+        with open(all_out, "w") as f:
             for d in out:
                 f.write(json.dumps(d) + "\n")
 
@@ -706,6 +705,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
+    ap.add_argument("--all-out", default=None, help="also write the --all records here, one JSON object a line")
     ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
