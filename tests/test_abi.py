@@ -31,8 +31,24 @@ def declared_functions():
 def test_header_declares_the_boundary_calls():
     names = declared_functions()
     for want in ["q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16", "q2k_mmvq_q8_1", "q2k_mmvq_pair",
-                 "q2k_mmvq_experts", "dense_gemm_bf16", "swiglu_q8_1_rows", "q2k_moe_m1"]:
+                 "q2k_mmvq_experts", "dense_gemm_bf16", "swiglu_q8_1_rows", "q2k_moe_m1", "q2k_mmvq_grouped",
+                 "q2k_engram_hash", "q3k_mmvq_q8_1", "q3k_mmvq_experts"]:
         assert want in names
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
+    # the boundary is usable from C: no C++ or CUDA types in the signatures
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use." + ("c" if lang == "c" else "cpp"))
+    src.write_text('#include "q2k.h"\nint main(void) { return (int)q2k_row_bytes(256) + (int)q3k_row_bytes(256); }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_library_exports_every_declared_symbol(L):
