@@ -545,3 +545,22 @@ def test_q3k_matvec_equals_numpy_matmul_of_decoded_matrix(N, K, m):
     np.testing.assert_allclose(oracle.q3k_matvec(W, N, K, x), x @ Wd.T, rtol=1e-12, atol=1e-12)
     # block b of row n decodes on its own
     np.testing.assert_array_equal(Wd[N - 1, K - 256:], oracle.q3k_decode_block(W[N - 1, -110:]))
+
+
+def test_round_bf16_is_fp32_then_bf16_nearest_even():
+    # the SwiGLU and expert rows are fp32 values rounded to bf16: the oracle's
+    # fp64 -> bf16 goes through fp32 the same way (two round-to-nearest-even steps)
+    rng = np.random.default_rng(41)
+    v = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 6, 2000),
+                        [0.0, -0.0, 1.0, -1.5, 3.0e38, 1e-40]])
+    # halfway cases at the bf16 step: exact ties go to the even mantissa
+    base = np.float32(1.0) + np.float32(2.0 ** -7) * np.arange(8, dtype=np.float32)
+    ties = (base.astype(np.float64) + 2.0 ** -8)
+    v = np.concatenate([v, ties, -ties])
+    got = oracle.round_bf16(v)
+    want = np.array([oracle.f32_to_bf16(float(np.float32(x))) for x in v], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+    # ties: 1 + k*2^-7 + 2^-8 rounds to the even k
+    tb = oracle.round_bf16(ties)
+    assert list((tb & 1).astype(int)) == [0] * 8
+    assert list(tb) == [0x3F80 + k + (k & 1) for k in range(8)]
