@@ -564,3 +564,24 @@ def test_round_bf16_is_fp32_then_bf16_nearest_even():
     tb = oracle.round_bf16(ties)
     assert list((tb & 1).astype(int)) == [0] * 8
     assert list(tb) == [0x3F80 + k + (k & 1) for k in range(8)]
+
+
+def test_engram_rows_projection_order_and_orientation():
+    # engram_v41.rs: rows are gathered in [token][col] order and viewed as
+    # [tokens, cols*256]; y = x wkv^T.  A permutation matrix as wkv returns
+    # each token's row back with its values permuted, exactly.
+    tokens, cols, n_table = 3, 2, 10
+    table = synth.q2k_blocks(5, "pin.engram", n_table)
+    ids = np.array([7, 2, 2, 9, 0, 5], dtype=np.int32)
+    K = cols * 256
+    perm = np.random.default_rng(5).permutation(K)
+    wkv = np.zeros((K, K), dtype=np.uint16)
+    wkv[np.arange(K), perm] = 0x3F80  # bf16 1.0: y[:, n] = x[:, perm[n]]
+    rows, y = oracle.engram_rows_projection(table, n_table, ids, tokens, cols, wkv)
+    for t in range(tokens):
+        for c in range(cols):
+            blk = table[ids[t * cols + c]]
+            np.testing.assert_array_equal(rows[t * cols + c], [oracle.f32_to_bf16(float(np.float32(w)))
+                                                               for w in oracle.decode_block(blk)])
+    x = oracle.bf16_to_f64(rows.reshape(tokens, K))
+    np.testing.assert_array_equal(y, x[:, perm])
