@@ -79,6 +79,18 @@ def test_q3k_mmvq_long_rows_many_chunks(lib, m):
     assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= TOL_EXACT_X
 
 
+@pytest.mark.parametrize("m", [1, 2])
+def test_q3k_mmvq_largest_k(lib, m):
+    # K = 2^20, the largest the boundary accepts: 4096 block columns, 256
+    # (one token) or 512 chunks per row, two or three rows per CTA
+    N, K = 3, 1 << 20
+    W = synth.q3k_matrix(11, "q3.maxk", N, K)
+    x = synth.bf16_normal(11, f"q3.maxk.x{m}", (m, K))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q3k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= TOL_EXACT_X
+
+
 @pytest.mark.parametrize("K", [512, 4096, 4864])
 def test_q3k_mmvq_weights_off_a_16_byte_boundary(lib, K):
     # the matrix starts 4 bytes into its buffer: every block's word phase flips
