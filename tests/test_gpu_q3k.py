@@ -50,7 +50,7 @@ def x_f64(bits):
 
 
 # slice widths 16/8/4 bytes, ragged chunks (nb not a multiple of the chunk),
-# one and several chunks per warp, every token count (5..8 take two launches)
+# one and several chunks per warp, every token count (pairs of tokens walk the rows in turn)
 CASES = [(1, 256, 1), (7, 512, 1), (33, 2048, 1), (300, 4096, 1), (65, 4864, 1), (40, 6400, 1),
          (33, 2048, 2), (300, 4096, 2), (65, 4864, 2), (31, 768, 3), (64, 4096, 4), (300, 1280, 4),
          (65, 4864, 5), (33, 2048, 6), (300, 4096, 8), (17, 256, 8)]
@@ -70,7 +70,7 @@ def test_q3k_mmvq_against_oracle(lib, N, K, m):
 
 @pytest.mark.parametrize("m", [1, 3])
 def test_q3k_mmvq_long_rows_many_chunks(lib, m):
-    # 256 block columns: 16 (one token) or 64 chunks, more than the 8 warps
+    # 256 block columns: 16 (one token) or 32 chunks, more than the 8 warps
     N, K = 40, 65536
     W = synth.q3k_matrix(4, "q3.long", N, K)
     x = synth.bf16_normal(4, f"q3.long.x{m}", (m, K))
@@ -82,7 +82,7 @@ def test_q3k_mmvq_long_rows_many_chunks(lib, m):
 @pytest.mark.parametrize("m", [1, 2])
 def test_q3k_mmvq_largest_k(lib, m):
     # K = 2^20, the largest the boundary accepts: 4096 block columns, 256
-    # (one token) or 512 chunks per row, two or three rows per CTA
+    # (one token) or 512 chunks per row, one row per CTA
     N, K = 3, 1 << 20
     W = synth.q3k_matrix(11, "q3.maxk", N, K)
     x = synth.bf16_normal(11, f"q3.maxk.x{m}", (m, K))
