@@ -21,9 +21,10 @@
 //    aligned), issued one row ahead so they overlap the arithmetic; the
 //    lanes then read their fields from shared memory.  Read straight from
 //    global memory, each lane's scattered 32-bit reads cost an L1 wavefront
-//    per sector.  What bounds the kernel now is the same unit: the lanes'
-//    word reads of 16 blocks 110 bytes apart meet in the same banks (about
-//    3.6 wavefronts per read), with issue about two thirds busy.
+//    per sector.  The lanes' word reads of 16 blocks 110 bytes apart still
+//    meet in the same banks (about 3.6 wavefronts per read), but a layout
+//    with half the conflicts ran no faster: the latency of those reads,
+//    with 16 warps per SM and issue about two thirds busy, is what binds.
 //    Only __syncwarp orders the buffer: no waits between warps or CTAs.
 //  * Blocks are 110 bytes, so every other block starts 2 bytes off a word:
 //    fields are read as aligned words and funnel-shifted.
