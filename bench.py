@@ -15,8 +15,10 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   region.
 * e2e repeats the metric with host buffers: each step copies the weights
   and x from pinned host memory, calls the C ABI, and reads y back.
-* cpu_baseline times the CPU oracle (one thread) on a bounded sample.
-* --impl reference times the CPU oracle on the same workload (rank 0 only).
+* cpu_baseline times the CPU oracle on a bounded sample, on one host thread and
+  on every host core (threads over output rows; the line's value).
+* --impl reference times the CPU oracle on the same workload on every host
+  core (rank 0 only).
 * --ncu-case [mv|mt|gemm|small|q3k] runs a few untimed calls for a profiler
   capture and prints no JSON line: mv = the headline kernel (bf16 GEMV) and
   the q8_1 MMVQ at m=1 on the headline shape; mt = the same shape at m=8
@@ -333,21 +335,59 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(W, x, budget_s: float = 20.0):
-    """The oracle (one thread) on a bounded sample of the headline workload:
-    rows of W until about budget_s seconds of CPU work."""
+def host_cores() -> int:
+    """Cores this process may run on (nproc)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_matvec_threads(W, xf, threads: int):
+    """The oracle's matvec over the rows of W, split into `threads`
+    contiguous row ranges run side by side (each range is one unchanged
+    oracle call; the C call releases the GIL).  Returns y [m, rows]."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    n = W.shape[0]
+    bounds = np.linspace(0, n, threads + 1).astype(int)
+    parts = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+    def one(ab):
+        a, b = ab
+        return oracle.matvec(np.ascontiguousarray(W[a:b]), b - a, K_HEAD, xf)
+
+    if len(parts) == 1:
+        return one(parts[0])
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        return np.concatenate(list(ex.map(one, parts)), axis=1)
+
+
+def cpu_baseline(W, x, budget_s: float = 10.0):
+    """The oracle on a bounded sample of the headline workload, on one host
+    thread and on every host core (threads over output rows): rows of W until
+    about budget_s seconds of single-thread CPU work.  The all-cores figure
+    is the line's value; `cores` is the threads it used, `host_cores` nproc."""
     xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    oracle_matvec_threads(W[:8], xf, 1)  # loads the oracle library
     rows = 64
     t0 = time.perf_counter()
-    oracle.matvec(np.ascontiguousarray(W[:rows]), rows, K_HEAD, xf)
+    oracle_matvec_threads(W[:rows], xf, 1)
     t_row = (time.perf_counter() - t0) / rows
     n = int(min(N_HEAD, max(rows, budget_s / max(t_row, 1e-9))))
     t0 = time.perf_counter()
-    oracle.matvec(np.ascontiguousarray(W[:n]), n, K_HEAD, xf)
-    dt = time.perf_counter() - t0
-    return {"value": n * (K_HEAD // 256) * 84 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n} of {N_HEAD} rows of the N=K=16384 m=1 workload ({dt:.1f} s)"}
+    y1 = oracle_matvec_threads(W[:n], xf, 1)
+    dt1 = time.perf_counter() - t0
+    nc = host_cores()
+    t0 = time.perf_counter()
+    yn = oracle_matvec_threads(W[:n], xf, nc)
+    dtn = time.perf_counter() - t0
+    assert np.array_equal(y1, yn)  # the row split leaves every row's arithmetic as it was
+    gb = n * (K_HEAD // 256) * 84 / 1e9
+    return {"value": gb / dtn, "unit": "GB/s", "cores": nc, "host_cores": nc, "kind": "oracle",
+            "sample": f"first {n} of {N_HEAD} rows of the N=K=16384 m=1 workload, {nc} threads over rows "
+                      f"({dtn:.2f} s)",
+            "single_thread": {"value": gb / dt1, "unit": "GB/s", "threads": 1, "seconds": dt1}}
 
 
 # ---- sweep over every configuration (--all) ------------------------------------------------
@@ -582,28 +622,31 @@ def run_reference(args):
     W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
     x = synth.bf16_normal(0, "sweep.x1", (1, K_HEAD))
     xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    nc = host_cores()
+    oracle_matvec_threads(W[:8], xf, 1)  # loads the oracle library
     t0 = time.perf_counter()
-    oracle.matvec(np.ascontiguousarray(W[:16]), 16, K_HEAD, xf)
-    t_row = (time.perf_counter() - t0) / 16
+    oracle_matvec_threads(W[:16 * nc], xf, nc)
+    t_row = (time.perf_counter() - t0) / (16 * nc)  # wall time per row on every core
     budget = 150.0  # seconds for warm-up + timed steps together
-    rows = int(max(1, min(N_HEAD, budget / max(1, args.steps + args.warmup) / max(t_row, 1e-9))))
+    rows = int(max(nc, min(N_HEAD, budget / max(1, args.steps + args.warmup) / max(t_row, 1e-9))))
     sample = np.ascontiguousarray(W[:rows])
     for _ in range(args.warmup):
-        oracle.matvec(sample, rows, K_HEAD, xf)
+        oracle_matvec_threads(sample, xf, nc)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.matvec(sample, rows, K_HEAD, xf)
+        oracle_matvec_threads(sample, xf, nc)
     dt = time.perf_counter() - t0
     value = args.steps * rows * (K_HEAD // 256) * 84 / dt / 1e9
-    desc = f"{rows} of {N_HEAD} rows of the N=K=16384 m=1 workload per step"
+    desc = f"{rows} of {N_HEAD} rows of the N=K=16384 m=1 workload per step, {nc} threads over rows"
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": "q2k_gemv_bf16 m=1 N=K=16384 (Q2_K weights, bf16 x) - CPU oracle sample",
-                   "parallelism": "single host thread"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+                   "parallelism": f"{nc} host threads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nc, "host_cores": nc, "kind": "oracle",
+                         "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -137,7 +137,10 @@ int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx
 /* Q2_K GEMV with bf16 activations, m = 1..8 tokens (engram_v41/apply.rs,
  * the single-token `engram_v41_wkv_q2k_gemv` off `wkv_q2k`).
  *   W  Q2_K [N, K];  x  bf16 [m, K], row stride ldx;  y  fp32 [m, N], row
- *   stride ldy.  y[t, n] = sum_k w[n, k] x[t, k], fp32 accumulation.
+ *   stride ldy.  y[t, n] = sum_k w[n, k] x[t, k]: exact int32 dot products
+ *   of the 2-bit codes with fixed-point activations per sub-block, scaled
+ *   by d, the sub-block scales and the activation exponents and summed in
+ *   fp32 (the bf16 values are not multiplied as floats).
  * The activations enter the integer dot products as 16-bit fixed point
  * with one power-of-two exponent per 16 values (exact unless a group spans
  * more than 2^7 in magnitude; then the smallest lose bits below 2^-15 of
@@ -203,9 +206,10 @@ int q2k_mmvq_grouped(const void* W, int64_t groups, int64_t rows_per_group, int6
  *                matrix gets CTAs of its own and the sum is a second
  *                launch over y; the bits are the same.
  *                Without y the sum is fused: each CTA keeps the partial
- *                sums of all n_mat matrices for its rows in shared memory,
- *                and a problem whose partials do not fit fails with a CUDA
- *                configuration error (pass y for many small matrices).
+ *                sums of all n_mat matrices for its rows in shared memory;
+ *                a problem whose partials do not fit returns
+ *                Q2K_ERR_WORKSPACE before any launch (pass y, which then
+ *                holds the per-matrix outputs, for many small matrices).
  * Gate and up run as one batch of 2*topk matrices; down as topk matrices
  * with x_per_matrix = 1 (moe_v41/init.rs, the `gate_out` comment). */
 int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64_t K,
@@ -292,7 +296,10 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,
  * Q2K_ERR_WORKSPACE before anything is enqueued (E = 8, dim = 4096,
  * inter = 2048 needs 285,184 bytes).  The first call on each device looks
  * the scratch's address up (cudaGetSymbolAddress, which may load the
- * module); make that first call before any stream capture.  Calls that
+ * module) and keeps it for the life of the process; make that first call
+ * before any stream capture.  A cudaDeviceReset invalidates the kept
+ * address: do not call this entry point on a device after resetting it.
+ * Shapes q2k_moe_m1 refuses return Q2K_ERR_BAD_SHAPE here too.  Calls that
  * overlap on one device share the scratch and race: issue them on one
  * stream.  Results equal q2k_moe_m1's bit for bit. */
 int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter,

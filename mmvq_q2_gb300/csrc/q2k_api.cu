@@ -399,6 +399,11 @@ int q2k_mmvq_experts(const void* const* W_table, int64_t n_mat, int64_t N, int64
             return e != cudaSuccess ? fail_cuda(e) : finish(e);
         return finish(launch_expert_sum(y, route_w, n_mat, N, y_sum, s));
     }
+    // the fused sum keeps every matrix's partial sums of a CTA's rows in
+    // shared memory: refuse, before any launch, a problem whose partials do
+    // not fit (per-matrix outputs in y are then the workspace it needs)
+    if (!mv_plan_ok(p))
+        return Q2K_ERR_WORKSPACE;
     return finish(launch_mv(p, s));
 }
 
@@ -577,7 +582,7 @@ int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const 
 // only this library and has no device allocator of its own, or a decode loop
 // whose memory is planned once up front and must not allocate (or make its
 // allocator grow) between steps.  For them this entry point runs the same
-// four launches as q2k_moe_m1 on a fixed scratch buffer that lives in the
+// launches as q2k_moe_m1 on a fixed scratch buffer that lives in the
 // library's own device image.  The scratch is a file-scope __device__ array,
 // so it is reserved when the module loads: nothing is allocated or freed here.
 //
@@ -595,6 +600,10 @@ std::mutex g_moe_scratch_mu;
 
 // The scratch's device address on the current device, looked up once per
 // device (the first call on a device does this; it may load the module).
+// The cached address belongs to the device's context at that time: after a
+// cudaDeviceReset the module loads again, possibly elsewhere, and the cached
+// address is stale, so a process that resets a device must not call this
+// entry point on it afterwards.
 cudaError_t moe_scratch(void** out)
 {
     int dev = 0;
@@ -621,9 +630,12 @@ extern "C" int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int
 {
     if (!ptrs || !x_bf16 || !route_w || !y)
         return Q2K_ERR_NULL_ARG;
-    const size_t need = q2k_moe_m1_workspace_bytes(E, dim, inter);
-    if (need == 0)
+    // the shapes q2k_moe_m1 refuses are refused here the same way; only a
+    // valid problem that needs more than the fixed scratch is a WORKSPACE error
+    if (E <= 0 || E > 1024 || dim <= 0 || inter <= 0 || dim % kBlockWeights || inter % kBlockWeights ||
+        dim > kMaxK || inter > kMaxK)
         return Q2K_ERR_BAD_SHAPE;
+    const size_t need = q2k_moe_m1_workspace_bytes(E, dim, inter);
     if (need > (size_t)Q2K_MOE_M1_STATIC_SCRATCH_BYTES)
         return Q2K_ERR_WORKSPACE;  // the problem does not fit the fixed scratch
     int st = check_device();

@@ -54,6 +54,10 @@ struct MvProblem {
 };
 
 cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
+// True when every K chunk of the problem has a launch plan that fits the
+// device (shared memory for the ring and the partial sums); no CUDA call
+// besides the cached device query.
+bool mv_plan_ok(const MvProblem& p);
 // Several tokens (m = 2..8, explicit segments) on the tensor cores.
 bool mt_supported(const MvProblem& p);
 cudaError_t launch_mt(const MvProblem& p, cudaStream_t s);

@@ -1148,10 +1148,13 @@ size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
 }  // namespace
 
-cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
+namespace {
+
+// Plan (and, unless dry, launch) every K chunk of a problem for
+// q2k_mv_kernel.  A dry run makes no CUDA call besides the device query, so
+// every chunk's plan is checked before the first launch.
+cudaError_t run_mv(const MvProblem& p, cudaStream_t s, bool dry)
 {
-    if (mt_supported(p))
-        return launch_mt(p, s);  // several tokens: the tensor-core kernel
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess)
@@ -1294,11 +1297,32 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
         if (nst < 2)
             return cudaErrorInvalidConfiguration;
         a.nst_magic = (uint32_t)((0x100000000ull + (uint64_t)a.nst - 1) / (uint64_t)a.nst);
+        if (dry)
+            continue;
         err = dispatch(p.act, sw, mc, a, (int)grid, smem, s);
         if (err != cudaSuccess)
             return err;
     }
     return cudaSuccess;
+}
+
+}  // namespace
+
+bool mv_plan_ok(const MvProblem& p)
+{
+    if (mt_supported(p))
+        return true;
+    return run_mv(p, nullptr, true) == cudaSuccess;
+}
+
+cudaError_t launch_mv(const MvProblem& p, cudaStream_t s)
+{
+    if (mt_supported(p))
+        return launch_mt(p, s);  // several tokens: the tensor-core kernel
+    cudaError_t err = run_mv(p, s, true);  // every chunk planned before any launch
+    if (err != cudaSuccess)
+        return err;
+    return run_mv(p, s, false);
 }
 
 cudaError_t mv_error_word(int32_t* out, bool clear)

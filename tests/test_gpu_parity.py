@@ -536,6 +536,29 @@ def test_experts_one_matrix_per_cta_equals_fused_sum(lib, n_mat, N, K, fused):
     assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
 
 
+def test_experts_fused_sum_too_big_is_refused_before_any_launch(lib):
+    """Without y the fused sum keeps every matrix's partial sums of a CTA's
+    rows in shared memory; a batch whose partials cannot fit returns
+    Q2K_ERR_WORKSPACE at the call, and y_sum is left untouched."""
+    import ctypes
+    n_mat, N, K = 160, 64, 256
+    mats = [dev(synth.q2k_matrix(4, f"exm.{n_mat}.{e}", N, K)) for e in range(n_mat)]
+    xq = lib.q8_1_quantize_rows(bf16_dev(synth.bf16_normal(4, f"exm.x{n_mat}", (n_mat, K))))
+    wt = torch.full((n_mat,), 0.5, dtype=torch.float32, device="cuda")
+    tbl = lib.pointer_table(mats)
+    ysum = torch.full((N,), 7.0, dtype=torch.float32, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = lib.lib().q2k_mmvq_experts(P(tbl), n_mat, N, K, P(xq), 1, None, P(wt), P(ysum),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 6  # Q2K_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(ysum == 7.0)
+    # with y as the workspace the same batch runs
+    y, _ = lib.q2k_mmvq_experts(tbl, N, K, xq, x_per_matrix=True, route_w=wt, y_sum=ysum)
+    ref = 0.5 * y.double().sum(0)
+    assert torch.max(torch.abs(ysum.double() - ref)) <= 1e-5 * torch.linalg.norm(ref)
+
+
 def test_swiglu_q8_1_against_oracle(lib):
     E, N = 3, 2048
     g = np.random.default_rng(3).standard_normal((2 * E, N)).astype(np.float32) * 2

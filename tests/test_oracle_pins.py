@@ -81,7 +81,7 @@ def test_block_size_is_the_pages_84_bytes():
     assert oracle.block_bytes() == facts["q2k_block_bytes"] == 84
     assert 16 + 64 + 2 + 2 == facts["q2k_block_bytes"]
     assert facts["q2k_block_weights"] == oracle.Q2K_WEIGHTS
-    # "84 bytes per 256 weights, against 512 in bf16"
+    # a bf16 row of 256 weights takes 512 bytes, against the block's 84
     assert facts["bf16_bytes_per_256"] == 2 * facts["q2k_block_weights"]
     assert oracle.Q8_1_BYTES == 2 + 2 + 32
 
@@ -370,6 +370,119 @@ def test_moe_chain_single_expert_and_quantised_agreement():
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
     q = oracle.moe_m1(x, gate, up, down, w, dim, inter, quantized=True)["y"]
     assert np.max(np.abs(q - a)) / np.linalg.norm(a) < 1e-2
+
+
+# ---- the MoE chain on hand-built experts, written out in closed form ------------
+#
+# moe_v41/init.rs, MoeV41::new: gate and up form one expert batch over the
+# shared x, SwiGLU of (gate, up) is requantised to q8_1, the down batch reads
+# expert e's own h row, and the outputs are summed with the route weights.
+# The experts below are built so that every intermediate has a closed form:
+#   gate/up: every code 3, every sub-block scale 1 and min 0, dmin 0, so each
+#            weight of row i is 3*d_i; with x = e_k, g[i] = 3*d_i exactly;
+#            d is constant over each run of 32 rows (one q8_1 block of h);
+#   down:    row r holds a single weight 1, at column perm_e[r], so
+#            down_e[r] = h_e[perm_e[r]].
+# The d values use the full fp16 significand, so 3*d is not a bf16 value
+# and every bf16 rounding point changes the result.
+
+def _const_rows_q2k(d_rows, K):
+    nb = K // 256
+    rows = len(d_rows)
+    b = np.zeros((rows, nb, 84), dtype=np.uint8)
+    b[:, :, 0:16] = 0x01   # scale 1, min 0
+    b[:, :, 16:80] = 0xFF  # every code 3
+    b[:, :, 80:82] = np.asarray(d_rows, dtype=np.float16).view(np.uint8).reshape(rows, 1, 2)
+    return b.reshape(-1)
+
+
+def _permutation_q2k(cols, K):
+    """Row r has weight 1 at column cols[r], 0 elsewhere (d = 1, dmin = 0)."""
+    nb = K // 256
+    b = np.zeros((len(cols), nb, 84), dtype=np.uint8)
+    for r, c in enumerate(cols):
+        blk = b[r, c // 256]
+        p = c % 256
+        blk[p // 16] = 0x01
+        blk[16 + 32 * (p // 128) + p % 32] |= np.uint8(1 << (2 * ((p % 128) // 32)))
+        blk[80:82] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    return b.reshape(-1)
+
+
+def _bf16(v: float) -> Fraction:
+    """fp64 -> fp32 -> bf16, each step round to nearest even (exact rationals)."""
+    return frac_to_binary(frac_to_binary(Fraction(v), 24, -126), 8, -126)
+
+
+def _q8_1_const_block(v: float) -> float:
+    """The value a q8_1 block whose 32 entries all equal v decodes to:
+    amax = |v|, d32 = amax/127 (fp32 divide), q = round(v/d32) = +-127,
+    stored d = fp16(d32); the decoded entry is f32(d) * q."""
+    if v == 0.0:
+        return 0.0
+    d32 = np.float32(abs(v)) / np.float32(127.0)
+    q = float(np.round(np.float32(v) / d32))
+    assert abs(q) == 127.0
+    return float(np.float16(d32)) * q
+
+
+def _moe_hand_case(seed=5, E=3, dim=512, inter=512):
+    g = np.random.default_rng(seed)
+    groups = inter // 32
+    dg = (g.uniform(0.1, 0.9, (E, groups)) * g.choice([-1.0, 1.0], (E, groups))).astype(np.float16)
+    du = (g.uniform(0.1, 0.9, (E, groups)) * g.choice([-1.0, 1.0], (E, groups))).astype(np.float16)
+    perms = [g.permutation(inter)[:dim] if dim <= inter else g.integers(0, inter, dim) for _ in range(E)]
+    gate = [_const_rows_q2k(np.repeat(dg[e], 32), dim) for e in range(E)]
+    up = [_const_rows_q2k(np.repeat(du[e], 32), dim) for e in range(E)]
+    down = [_permutation_q2k(perms[e], inter) for e in range(E)]
+    k = int(g.integers(0, dim))
+    x = np.zeros((1, dim), dtype=np.uint16)
+    x[0, k] = 0x3F80  # bf16 1.0
+    w = np.array(g.dirichlet(np.ones(E)), dtype=np.float32)
+    return dict(E=E, dim=dim, inter=inter, dg=dg, du=du, perms=perms, gate=gate, up=up, down=down, x=x, w=w)
+
+
+def _moe_expected(c, quantized):
+    """The chain written out: g, u rounded to bf16, h = bf16(silu(g) * u),
+    (q8_1 of x and of h when quantized), down_e = h_e[perm_e], y = sum_e w_e down_e."""
+    # x = e_k: its q8_1 block has amax 1, so x_k decodes as a constant block of 1s would
+    xk = _q8_1_const_block(1.0) if quantized else 1.0
+    out = {"g": [], "u": [], "h": [], "down": []}
+    y = np.zeros(c["dim"])
+    for e in range(c["E"]):
+        g = np.repeat(3.0 * c["dg"][e].astype(np.float64) * xk, 32)
+        u = np.repeat(3.0 * c["du"][e].astype(np.float64) * xk, 32)
+        g16 = np.array([float(_bf16(v)) for v in g])
+        u16 = np.array([float(_bf16(v)) for v in u])
+        silu = g16 / (1.0 + np.exp(-g16))
+        h = np.array([float(_bf16(v)) for v in silu * u16])
+        hin = np.array([_q8_1_const_block(v) for v in h]) if quantized else h
+        dn = hin[c["perms"][e]]
+        y = y + np.float64(c["w"][e]) * dn
+        for key, v in (("g", g), ("u", u), ("h", h), ("down", dn)):
+            out[key].append(v)
+    out["y"] = y
+    return out
+
+
+@pytest.mark.parametrize("quantized", [False, True])
+def test_moe_chain_on_hand_built_experts_matches_closed_form(quantized):
+    """Fails if silu lands on u instead of g, if a bf16 rounding of g, u or h
+    is dropped, if the down batch reads another expert's h (or reads h
+    through a transposed matrix), or if the route weights are misassigned."""
+    c = _moe_hand_case()
+    got = oracle.moe_m1(c["x"], c["gate"], c["up"], c["down"], c["w"], c["dim"], c["inter"], quantized=quantized)
+    exp = _moe_expected(c, quantized)
+    np.testing.assert_array_equal(got["g"], np.stack(exp["g"]))
+    np.testing.assert_array_equal(got["u"], np.stack(exp["u"]))
+    np.testing.assert_array_equal(oracle.bf16_to_f64(got["h_bits"]), np.stack(exp["h"]))
+    np.testing.assert_array_equal(got["down"], np.stack(exp["down"]))
+    np.testing.assert_allclose(got["y"], exp["y"], rtol=1e-15, atol=0)
+    # every rounding point and role matters on this case: the alternatives differ
+    g16 = np.array([float(_bf16(v)) for v in exp["g"][0]])
+    u16 = np.array([float(_bf16(v)) for v in exp["u"][0]])
+    assert not np.array_equal(g16, exp["g"][0]) and not np.array_equal(u16, exp["u"][0])
+    assert not np.allclose(g16 / (1 + np.exp(-g16)) * u16, u16 / (1 + np.exp(-u16)) * g16, rtol=1e-3)
 
 
 # ---- engram n-gram hash (engram_v41.rs, EngramHasher::hash) ---------------------
