@@ -68,7 +68,7 @@ def peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("q2k_mv.cu", "q2k_common.cuh"):
+    for f in ("q2k_m1.cu", "q2k_slice.cuh", "q2k_common.cuh"):
         h.update(open(os.path.join(ROOT, "mmvq_q2_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -58,6 +58,11 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
 // device (shared memory for the ring and the partial sums); no CUDA call
 // besides the cached device query.
 bool mv_plan_ok(const MvProblem& p);
+// One token over rows of 32..128 blocks (K % 1024 == 0, 16-byte aligned
+// weights and activations), one or two explicit segments: per-team rings of
+// one-row stages (q2k_m1.cu).
+bool m1_supported(const MvProblem& p);
+cudaError_t launch_m1(const MvProblem& p, cudaStream_t s);
 // Several tokens (m = 2..8, explicit segments) on the tensor cores.
 bool mt_supported(const MvProblem& p);
 cudaError_t launch_mt(const MvProblem& p, cudaStream_t s);
@@ -101,6 +106,7 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s);
 
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
+cudaError_t m1_error_word(int32_t* out, bool clear);
 cudaError_t gemm_error_word(int32_t* out, bool clear);
 cudaError_t mt_error_word(int32_t* out, bool clear);
 cudaError_t umma_error_word(int32_t* out, bool clear);
