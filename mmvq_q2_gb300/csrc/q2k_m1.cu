@@ -8,14 +8,16 @@
 // a fixed 128-weight slice of every row and keeps the matching activations
 // in registers (q2k_slice.cuh).
 //
-// Weight stream.  A stage is one row per team: T consecutive rows of the
-// CTA's range (about 21 KB), so it arrives with a single 1-D bulk copy.  The
+// Weight stream.  A stage is two rows per team: 2T consecutive rows of the
+// CTA's range (about 43 KB), so it arrives with a single 1-D bulk copy.  The
 // copy size is what sets the stream rate on this part: rings of 1.3 KB or
-// 5 KB copies stream the 16384^2 matrix at 3.6 and 4.3 TB/s, 21 KB copies
-// at 6.3 TB/s (the same as plain 16-byte loads).  The weights do not depend
-// on the activations, so the whole ring (8 stages, about 170 KB) is
-// requested right after the launch's dependency wait, before the
-// activations are staged, and covers the activation prologue.
+// 5 KB copies stream the 16384^2 matrix at 3.6 and 4.3 TB/s, 21 KB and
+// 43 KB copies at 6.3 and 6.4 TB/s (plain 16-byte loads: 6.15).  Two rows
+// per team also halve the per-row cost of waiting for and releasing a
+// stage.  The weights do not depend on the activations, so the whole ring
+// (4 stages, about 170 KB) is requested right after the launch's dependency
+// wait, before the activations are staged, and covers the activation
+// prologue.
 //
 // Release and refill.  A warp done with a stage counts itself out on the
 // slot's counter in shared memory (lane 0, one atomic add); the warp that
@@ -45,6 +47,7 @@ namespace {
 constexpr int kM1Threads = 512;  // 16 warps of row teams
 constexpr int kM1Warps = kM1Threads / 32;
 constexpr int kM1Rpt = 4;  // rows per lane between two reductions
+constexpr int kM1Rps = 2;  // rows per team in a stage
 
 struct M1Args {
     const uint8_t* W[2];  // row space: rows [0, N0) of W[0], then rows of W[1]
@@ -55,11 +58,11 @@ struct M1Args {
     int nb;              // Q2_K blocks per row
     int lanes;           // lanes per row team: a power of two >= 2 * nb, 32..512
     int log_lanes;
-    int teams;           // kM1Threads / lanes = rows per stage
+    int teams;           // kM1Threads / lanes
     int wpt;             // warps per team (lanes / 32)
     int depth;           // stages in the ring
     uint32_t row_bytes;  // nb * 84, a multiple of 16
-    uint32_t stage_bytes;  // teams * row_bytes
+    uint32_t stage_bytes;  // kM1Rps * teams * row_bytes
     const uint8_t* x;    // bf16 row or q8_1 row
     uint32_t x_bytes;
     uint32_t off_x, off_bar, off_red;
@@ -96,7 +99,8 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
     const int cta = (int)blockIdx.x;
     const int lo = cta * a.rows_q + min(cta, a.rows_r);
     const int hi = lo + a.rows_q + (cta < a.rows_r ? 1 : 0);
-    const int nst = (hi - lo + a.teams - 1) / a.teams;  // stage j: rows lo + teams*j + t
+    const int spr = kM1Rps * a.teams;        // rows per stage
+    const int nst = (hi - lo + spr - 1) / spr;  // stage j: rows lo + spr*j + Rps*t + q
 
     if (tid == 0) {
         mbar_init(smem_u32(xbar), 1);
@@ -115,8 +119,8 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
 
     // ---- stage j into slot s = j % depth (one thread) ----
     auto issue = [&](int j, int s) {
-        const int r0 = lo + a.teams * j;
-        const int r1 = min(hi, r0 + a.teams);
+        const int r0 = lo + spr * j;
+        const int r1 = min(hi, r0 + spr);
         const uint32_t fb = smem_u32(&full_b[s]);
         uint8_t* dst = ring + (size_t)s * a.stage_bytes;
         const uint64_t pol = l2_policy_evict_first();  // the weights are read once
@@ -165,26 +169,29 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
     {
         load_slice<1, ACT, 8>(sl, xsm, a.nb, b, n, 0, active);
 
-        const uint8_t* blk0 = ring + (size_t)team * a.row_bytes + (size_t)b * kBlockBytes;
+        const uint8_t* blk0 = ring + (size_t)team * kM1Rps * a.row_bytes + (size_t)b * kBlockBytes;
         // stage j's slot, the parity of its phase there, j / depth and this
-        // team's row, advanced one stage at a time (no divisions)
-        int s = 0, kd = 0, row = lo + team;
+        // team's first row, advanced one stage at a time (no divisions)
+        int s = 0, kd = 0, row = lo + kM1Rps * team;
         uint32_t parity = 0;
         // the previous stage (its slot, and the count the last warp out of it
         // sees) and, in lane 0, what this warp's atomic returned for it
         int prev_j = -1, prev_s = 0, prev_last = 0, prev_count = 0;
-        // One stage: wait, this team's row, count the warp out; the
+        // One stage: wait, this team's rows, count the warp out; the
         // previous stage's count has come back by now, and the warp that was
-        // last out of it refills its slot.  TAIL: the stage may lack a row
-        // for this team (the CTA's last stage).
-        auto stage = [&](int j, bool tail) -> float {
-            float v = 0.f;
+        // last out of it refills its slot.  TAIL: the stage may lack rows for
+        // this team (the CTA's last stage).
+        auto stage = [&](int j, bool tail, float* v) {
             if (!aborted && !wait(smem_u32(&full_b[s]), parity))
                 aborted = true;
-            if (!aborted && (!tail || row < hi)) {
-                float acc[1] = {0.f};
-                slice_dot<1, ACT, 8>(sl, blk0 + (size_t)s * a.stage_bytes, n, 0, acc);
-                v = acc[0];
+#pragma unroll
+            for (int q = 0; q < kM1Rps; ++q) {
+                v[q] = 0.f;
+                if (!aborted && (!tail || row + q < hi)) {
+                    float acc[1] = {0.f};
+                    slice_dot<1, ACT, 8>(sl, blk0 + (size_t)s * a.stage_bytes + (size_t)q * a.row_bytes, n, 0, acc);
+                    v[q] = acc[0];
+                }
             }
             __syncwarp();
             if (lane == 0) {
@@ -197,35 +204,44 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
             prev_j = j;
             prev_s = s;
             prev_last = kM1Warps * (kd + 1) - 1;
-            row += a.teams;
+            row += spr;
             if (++s == a.depth) {
                 s = 0;
                 parity ^= 1u;
                 ++kd;
             }
-            return v;
         };
-        // each lane group of 8 ends up with one row's warp partial
+        // value k of v is row Rps*t + (k % Rps) of stage j0 + k / Rps; each
+        // lane group of 8 ends up with one row's warp partial
+        constexpr int SPG = kM1Rpt / kM1Rps;  // stages per reduction group
         auto deposit = [&](int j0, float (&v)[kM1Rpt]) {
             const float r = transpose_reduce<kM1Rpt>(v, lane);
-            const int rl = a.teams * (j0 + (lane >> 3)) + team;  // row within the CTA's range
+            const int k = lane >> 3;
+            const int rl = spr * (j0 + k / kM1Rps) + kM1Rps * team + k % kM1Rps;  // row within the CTA's range
             if ((lane & 7) == 0 && lo + rl < hi)
                 red[(size_t)rl * a.wpt + wit] = r;
         };
-        const int nst_full = (hi - lo) / a.teams;  // stages with a row for every team
+        const int nst_full = (hi - lo) / spr;  // stages with every row present
         int j0 = 0;
-        for (; j0 + kM1Rpt <= nst_full; j0 += kM1Rpt) {
+        for (; j0 + SPG <= nst_full; j0 += SPG) {
             float v[kM1Rpt];
 #pragma unroll
-            for (int k = 0; k < kM1Rpt; ++k)
-                v[k] = stage(j0 + k, false);
+            for (int g = 0; g < SPG; ++g)
+                stage(j0 + g, false, v + g * kM1Rps);
             deposit(j0, v);
         }
-        if (j0 < nst) {
+        for (; j0 < nst; j0 += SPG) {
             float v[kM1Rpt];
 #pragma unroll
-            for (int k = 0; k < kM1Rpt; ++k)
-                v[k] = j0 + k < nst ? stage(j0 + k, true) : 0.f;
+            for (int g = 0; g < SPG; ++g) {
+                if (j0 + g < nst) {
+                    stage(j0 + g, true, v + g * kM1Rps);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kM1Rps; ++q)
+                        v[g * kM1Rps + q] = 0.f;
+                }
+            }
             deposit(j0, v);
         }
         // the last stage's count needs no refill: nothing is left to load
@@ -293,7 +309,7 @@ bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, siz
     a.teams = kM1Threads / a.lanes;
     a.wpt = a.lanes / 32;
     a.row_bytes = (uint32_t)(a.nb * kBlockBytes);
-    a.stage_bytes = (uint32_t)a.teams * a.row_bytes;
+    a.stage_bytes = (uint32_t)(kM1Rps * a.teams) * a.row_bytes;
     a.W[0] = static_cast<const uint8_t*>(p.W[0]);
     a.W[1] = static_cast<const uint8_t*>(nseg > 1 ? p.W[1] : p.W[0]);
     a.y[0] = p.y[0];
@@ -314,7 +330,8 @@ bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, siz
         a.off_bar = (uint32_t)(a.off_x + x_region);
         a.off_red = (uint32_t)align16(a.off_bar + (size_t)(depth + 2) * sizeof(uint64_t) +
                                       (size_t)(2 * depth) * sizeof(int));
-        smem = align16(a.off_red + (size_t)a.teams * ((rows_cta + a.teams - 1) / a.teams) * a.wpt * sizeof(float));
+        const int spr = kM1Rps * a.teams;
+        smem = align16(a.off_red + (size_t)spr * ((rows_cta + spr - 1) / spr) * a.wpt * sizeof(float));
         if (smem <= cap)
             return true;
     }
