@@ -589,6 +589,27 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 + 16 * 20480 * 4, 16)
     del wkvs
 
+    # the page's single-token engram path (engram_v41/apply.rs, `apply`: one
+    # token reads `wkv_q2k`): hash of the decode token -> its 8 row ids ->
+    # rows -> the Q2_K GEMV against wkv_q2k [20480, 2048]
+    wq = synth.q2k_matrix(0, "engram.wkv_q2k", 20480, 2048)
+    R = copies_for(wq.nbytes, l2)
+    wqs = [torch.from_numpy(wq).cuda() for _ in range(R)]
+    rows1 = torch.empty((8, 256), dtype=torch.int16, device="cuda")
+    y1 = torch.empty((1, 20480), dtype=torch.float32, device="cuda")
+    lids1 = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+    hout1 = torch.empty((1, 2, 8), dtype=torch.int64, device="cuda")
+
+    def engram_one(i):
+        check(L.q2k_engram_hash(P(tm), tm.numel(), P(hc), hc.numel(), P(toks), 1, 16, 3, 2, 4, P(mults), P(primes),
+                                P(offs), 0, P(hout1), P(lids1), 1, None, cur()), "hash")
+        check(L.q2k_dequant_rows(P(table), n_table, 256, P(lids1), 8, P(rows1), None, cur()), "dequant")
+        check(L.q2k_gemv_bf16(P(wqs[i % R]), 20480, 2048, P(rows1), 1, 2048, P(y1), 20480, cur()), "gemv")
+    el, n = graph_time(engram_one, 2000, 100)
+    rec("engram one token: hash + rows(8) + q2k_gemv_bf16 [20480x2048] (wkv_q2k)", el / n,
+        wq.nbytes + 8 * 84 + 2 * 8 * 256 * 2 + 20480 * 4, 1, {"launches_per_call": 3})
+    del wqs
+
     # cfg4: dense GEMM m in {64, 256}
     for Nn in (4096, 8192, 16384):
         Wdn = synth.bf16_normal(0, f"sweep.dense.W{Nn}", (Nn, Nn), std=0.02)
