@@ -608,7 +608,31 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     el, n = graph_time(engram_one, 2000, 100)
     rec("engram one token: hash + rows(8) + q2k_gemv_bf16 [20480x2048] (wkv_q2k)", el / n,
         wq.nbytes + 8 * 84 + 2 * 8 * 256 * 2 + 20480 * 4, 1, {"launches_per_call": 3})
+
+    # the whole engram step: the same chains, then the gate on the fp32
+    # streams [T, hc=4, dim=4096] (engram_v41.rs module doc, step 4)
+    qk = torch.from_numpy(np.random.default_rng(2).uniform(0.5, 1.5, (4, 4096)).astype(np.float32)).cuda()
+    st1 = torch.from_numpy(np.random.default_rng(3).standard_normal((1, 4, 4096)).astype(np.float32)).cuda()
+    st16 = torch.from_numpy(np.random.default_rng(4).standard_normal((16, 4, 4096)).astype(np.float32)).cuda()
+
+    def engram_step_one(i):
+        engram_one(i)
+        check(L.q2k_engram_gate(P(st1), P(y1), 20480, P(qk), 1, 4, 4096, ctypes.c_float(1e-6), None, cur()), "gate")
+    el, n = graph_time(engram_step_one, 2000, 100)
+    rec("engram step one token: hash + rows(8) + q2k_gemv_bf16 (wkv_q2k) + gate [4x4096]", el / n,
+        wq.nbytes + 8 * 84 + 2 * 8 * 256 * 2 + 20480 * 4 + 20480 * 4 + 3 * 4 * 4096 * 4, 1, {"launches_per_call": 4})
     del wqs
+    wkvs = [torch.from_numpy(wkv.view(np.int16)).cuda() for _ in range(copies_for(wkv.nbytes, l2))]
+    R = len(wkvs)
+
+    def engram_step16(i):
+        engram_chain(i)
+        check(L.q2k_engram_gate(P(st16), P(yk), 20480, P(qk), 16, 4, 4096, ctypes.c_float(1e-6), None, cur()), "gate")
+    el, n = graph_time(engram_step16, 500, 20)
+    rec("engram step 16 tokens: hash + rows(128) + dense_gemm m=16 + gate [16x4x4096]", el / n,
+        wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 + 16 * 20480 * 4 * 2 + 16 * 3 * 4 * 4096 * 4, 16,
+        {"launches_per_call": 4})
+    del wkvs
 
     # cfg4: dense GEMM m in {64, 256}
     for Nn in (4096, 8192, 16384):

@@ -126,6 +126,31 @@ int q2k_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, int
                     const int64_t* offsets, int64_t pad_id, int64_t* out, int32_t* layer_ids,
                     int64_t layer_index, int32_t* err_flag, q2k_stream_t stream);
 
+/* Engram gate (engram_v41.rs, module doc, step 4; engram_v41/apply.rs,
+ * `apply`, the `gate_k` launch over [tokens, hc] with streams, kv, qk, dim,
+ * hc, eps): a normalised dot of each stream against its key, a signed-sqrt
+ * sigmoid, and h += gate * value, in place on the fp32 streams.
+ *   streams  fp32 [tokens, hc, dim], contiguous; updated in place
+ *   kv       fp32 [tokens, ld_kv]: row t holds hc keys of dim values, then
+ *            the shared value (dim values): the projection's output
+ *            (engram_v41.rs, `out_features` = dim * (hc + 1)); every kv
+ *            value is rounded to bf16 before use, as the page's kv buffer
+ *            is bf16
+ *   ld_kv    floats between kv rows, >= (hc + 1) * dim
+ *   qk       fp32 [hc, dim]: q_weight * k_weight, elementwise
+ *            (engram_v41.rs, `EngramV41::upload_qk`)
+ *   gates    fp32 [tokens, hc], nullable: receives each gate
+ * For stream c of token t, with h the stream, k its key and v the value:
+ *   s = sum_i qk[c,i] h_i k_i / (rms(h) rms(k) sqrt(dim)),
+ *   rms(z) = sqrt(mean(z^2) + eps),  g = 1 / (1 + exp(-sign(s) sqrt(|s|))),
+ *   h_i += g v_i.
+ * The pages name these steps without their arithmetic; the 1/sqrt(dim)
+ * scale and the key/value order are this library's reading.  fp32, sums in
+ * a fixed order (a call repeats bit for bit).  1 <= hc <= 4 (the page's
+ * limit), 1 <= dim <= 2^20, eps >= 0.  One launch; tokens == 0 is a no-op. */
+int q2k_engram_gate(float* streams, const float* kv, int64_t ld_kv, const float* qk, int64_t tokens, int64_t hc,
+                    int64_t dim, float eps, float* gates, q2k_stream_t stream);
+
 /* Quantise bf16 rows to q8_1 (attn_v41/decode.rs, `kquant_q8_1_rows`;
  * moe_v41/init.rs, `kquant_q8_1_rows_bf16`).
  *   x_bf16   [m, K] with row stride ldx elements (ldx >= K); K % 32 == 0

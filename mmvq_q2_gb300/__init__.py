@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libq2k.so")
 
 # Every entry point include/q2k.h declares.
 EXPORTS = (
-    "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q2k_engram_hash", "q8_1_quantize_rows",
+    "q2k_row_bytes", "q8_1_row_bytes", "q2k_dequant_rows", "q2k_engram_hash", "q2k_engram_gate", "q8_1_quantize_rows",
     "q2k_gemv_bf16",
     "q2k_mmvq_q8_1", "q2k_mmvq_pair", "q2k_mmvq_pair_bf16", "q2k_mmvq_grouped", "q2k_mmvq_experts",
     "q3k_row_bytes", "q3k_mmvq_q8_1", "q3k_mmvq_experts",
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
             "q2k_dequant_rows": (I32, [P, I64, I64, P, I64, P, P, P]),
             "q8_1_quantize_rows": (I32, [P, I64, I64, I64, P, P]),
             "q2k_engram_hash": (I32, [P, I64, P, I64, P, I64, I64, I64, I64, I64, P, P, P, I64, P, P, I64, P, P]),
+            "q2k_engram_gate": (I32, [P, P, I64, P, I64, I64, I64, ctypes.c_float, P, P]),
             "q2k_gemv_bf16": (I32, [P, I64, I64, P, I64, I64, P, I64, P]),
             "q2k_mmvq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P]),
             "q2k_mmvq_pair": (I32, [P, I64, P, P, I64, P, I64, P, I64, P]),
@@ -163,6 +164,20 @@ def q8_1_quantize_rows(x, out=None, stream=None):
         out = torch.empty((m, q8_1_row_bytes(K)), dtype=torch.uint8, device=x.device)
     _call("q8_1_quantize_rows", _ptr(x), m, K, x.stride(0), _ptr(out), _stream(stream))
     return out
+
+
+def q2k_engram_gate(streams, kv, qk, eps, gates=None, stream=None):
+    """Engram gate in place on fp32 ``streams [T, hc, dim]`` from fp32
+    ``kv [T, >= (hc+1)*dim]`` (keys, then the shared value) and fp32
+    ``qk [hc, dim]``; returns ``streams`` (and fills ``gates [T, hc]`` when
+    given)."""
+    _need_cuda(streams, kv, qk, gates)
+    T, hc, dim = streams.shape
+    if not streams.is_contiguous() or kv.stride(1) != 1 or not qk.is_contiguous():
+        raise ValueError("streams and qk must be contiguous, kv rows dense")
+    _call("q2k_engram_gate", _ptr(streams), _ptr(kv), kv.stride(0), _ptr(qk), T, hc, dim, float(eps), _ptr(gates),
+          _stream(stream))
+    return streams
 
 
 def q2k_gemv_bf16(W, x, out=None, stream=None):

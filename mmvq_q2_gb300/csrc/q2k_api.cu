@@ -191,6 +191,25 @@ int q2k_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, int
                                      (int)layer_index, err_flag, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int q2k_engram_gate(float* streams, const float* kv, int64_t ld_kv, const float* qk, int64_t tokens, int64_t hc,
+                    int64_t dim, float eps, float* gates, q2k_stream_t stream)
+{
+    if (tokens > 0 && (!streams || !kv || !qk))
+        return Q2K_ERR_NULL_ARG;
+    if (tokens < 0 || tokens > (1 << 30) || hc < 1 || hc > 4 || dim < 1 || dim > kMaxK || ld_kv < (hc + 1) * dim ||
+        !(eps >= 0.f) || eps > 3.0e38f)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(streams, 4) || !aligned(kv, 4) || !aligned(qk, 4) || (gates && !aligned(gates, 4)))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (tokens == 0)
+        return Q2K_OK;
+    return finish(launch_engram_gate(streams, kv, ld_kv, qk, tokens, (int)hc, (int)dim, eps, gates,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx, void* out_q8_1,
                        q2k_stream_t stream)
 {

@@ -77,6 +77,9 @@ cudaError_t launch_engram_hash(const int64_t* token_map, int64_t vocab, int64_t*
                                int64_t seqlen, int64_t start_pos, int ng, int nl, int nh, const int64_t* mults,
                                const int64_t* primes, const int64_t* offsets, int64_t pad_id, int64_t* out,
                                int32_t* layer_ids, int layer_index, int32_t* err_flag, cudaStream_t s);
+// The engram gate over [tokens, hc] (q2k.h, q2k_engram_gate).
+cudaError_t launch_engram_gate(float* streams, const float* kv, int64_t ld_kv, const float* qk, int64_t tokens,
+                               int hc, int dim, float eps, float* gates, cudaStream_t s);
 // y_sum[n] = sum_e route_w[e] * y_exp[e][n], fp32 fmaf in e order from 0.
 cudaError_t launch_expert_sum(const float* y_exp, const float* route_w, int64_t E, int64_t N, float* y_sum,
                               cudaStream_t s);

@@ -3,7 +3,9 @@
 //    `dequant_q2_k_to_bf16`), with the row gather moved onto the device;
 //  - bf16 -> q8_1 rows (attn_v41/decode.rs, `kquant_q8_1_rows`);
 //  - SwiGLU fused with q8_1 requantisation (moe_v41/init.rs,
-//    `kquant_swiglu_q8_1_rows_bf16`).
+//    `kquant_swiglu_q8_1_rows_bf16`);
+//  - the engram n-gram hash (engram_v41.rs, `EngramHasher::hash`) and the
+//    engram gate (engram_v41.rs module doc, step 4).
 #include "q2k_common.cuh"
 #include "q2k_internal.h"
 #include "q2k_q8.cuh"
@@ -292,6 +294,80 @@ cudaError_t launch_engram_hash(const int64_t* token_map, int64_t vocab, int64_t*
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 1024));
     return launch_pdl(engram_hash_kernel, dim3((unsigned)grid), dim3(256), 0, s, token_map, vocab, cache, input_ids, seqlen,
                       start_pos, ng, nl, nh, mults, primes, offsets, pad_id, out, layer_ids, layer_index, err_flag);
+}
+
+// ---- engram gate ----------------------------------------------------------------
+// engram_v41.rs, module doc, step 4, and engram_v41/apply.rs, `apply` (the
+// `gate_k` launch over [tokens, hc]): one CTA per (token, stream).  The
+// stream h (fp32, dim values), its key k and the shared value v (kv row t:
+// keys 0..hc-1, then the value; each kv value rounded to bf16, the page's
+// kv buffer being bf16) give
+//   s = sum_i qk_i h_i k_i / (rms(h) rms(k) sqrt(dim)),
+//   rms(z) = sqrt(mean(z^2) + eps),  g = sigmoid(sign(s) sqrt(|s|)),
+// and h += g v in place.  The three sums are reduced in a fixed order, so a
+// call repeats bit for bit.
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+__global__ void __launch_bounds__(256) engram_gate_kernel(float* __restrict__ streams, const float* __restrict__ kv,
+                                                          int64_t ld_kv, const float* __restrict__ qk, int hc, int dim,
+                                                          float eps, float* __restrict__ gates)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int t = (int)blockIdx.x, c = (int)blockIdx.y;
+    float* h = streams + ((int64_t)t * hc + c) * dim;
+    const float* k = kv + (int64_t)t * ld_kv + (int64_t)c * dim;
+    const float* v = kv + (int64_t)t * ld_kv + (int64_t)hc * dim;
+    const float* q = qk + (int64_t)c * dim;
+    float shh = 0.f, skk = 0.f, shk = 0.f;
+    for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+        const float hv = h[i];
+        const float kk = bf16_round(k[i]);
+        shh = fmaf(hv, hv, shh);
+        skk = fmaf(kk, kk, skk);
+        shk = fmaf(q[i] * hv, kk, shk);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        shh += __shfl_xor_sync(0xffffffffu, shh, o);
+        skk += __shfl_xor_sync(0xffffffffu, skk, o);
+        shk += __shfl_xor_sync(0xffffffffu, shk, o);
+    }
+    __shared__ float part[3][8];
+    __shared__ float gate;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        part[0][warp] = shh;
+        part[1][warp] = skk;
+        part[2][warp] = shk;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.f, b = 0.f, d = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            a += part[0][w];
+            b += part[1][w];
+            d += part[2][w];
+        }
+        const float rh = sqrtf(a / (float)dim + eps);
+        const float rk = sqrtf(b / (float)dim + eps);
+        const float sc = d / (rh * rk * sqrtf((float)dim));
+        const float ss = copysignf(sqrtf(fabsf(sc)), sc);
+        gate = 1.f / (1.f + expf(-ss));
+        if (gates)
+            gates[(int64_t)t * hc + c] = gate;
+    }
+    __syncthreads();
+    const float g = gate;
+    for (int i = threadIdx.x; i < dim; i += blockDim.x)
+        h[i] = fmaf(g, bf16_round(v[i]), h[i]);
+}
+
+cudaError_t launch_engram_gate(float* streams, const float* kv, int64_t ld_kv, const float* qk, int64_t tokens,
+                               int hc, int dim, float eps, float* gates, cudaStream_t s)
+{
+    return launch_pdl(engram_gate_kernel, dim3((unsigned)tokens, (unsigned)hc), dim3(256), 0, s, streams, kv, ld_kv, qk,
+                      hc, dim, eps, gates);
 }
 
 }  // namespace q2k

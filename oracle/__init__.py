@@ -85,6 +85,7 @@ def _L():
             lib.oracle_engram_hash.restype = ctypes.c_int
             lib.oracle_engram_hash.argtypes = [P, I64, P, I64, P, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                P, P, P, I64, P]
+            lib.oracle_engram_gate.argtypes = [P, P, I64, P, I64, I64, I64, ctypes.c_float, P, P]
             lib.oracle_q3k_decode_block.argtypes = [P, P]
             lib.oracle_q3k_decode_matrix.argtypes = [P, I64, I64, P]
             lib.oracle_q3k_matvec.argtypes = [P, I64, I64, P, I64, P]
@@ -352,6 +353,24 @@ def engram_hash(token_map, cache, input_ids, start_pos, max_ngram, n_layers, n_h
     if st == -2:
         raise ValueError("positions past the hash cache")
     return out
+
+
+def engram_gate(streams, kv, qk, eps):
+    """The engram gate (engram_v41.rs module doc, step 4; engram_v41/apply.rs,
+    the `gate_k` launch): ``streams`` fp32 ``[T, hc, dim]``, ``kv`` fp32
+    ``[T, (hc+1)*dim]`` (keys, then the shared value; rounded to bf16 on
+    use), ``qk`` fp32 ``[hc, dim]``.  Returns ``(new streams fp64 [T, hc,
+    dim], gates fp64 [T, hc])``; the readings are in q2k_oracle.c."""
+    st = _c(streams, np.float32)
+    T, hc, dim = st.shape
+    kv = _c(kv, np.float32)
+    assert kv.shape[0] == T and kv.shape[1] >= (hc + 1) * dim
+    q = _c(qk, np.float32)
+    assert q.shape == (hc, dim)
+    out = np.empty((T, hc, dim), dtype=np.float64)
+    g = np.empty((T, hc), dtype=np.float64)
+    _L().oracle_engram_gate(_p(st), _p(kv), kv.shape[1], _p(q), T, hc, dim, float(np.float32(eps)), _p(out), _p(g))
+    return out, g
 
 
 def layer_row_ids(hashes, layer):

@@ -470,6 +470,55 @@ int oracle_engram_hash(const int64_t* token_map, int64_t vocab, int64_t* cache, 
     return 0;
 }
 
+/* ---- engram gate ---------------------------------------------------------
+ * engram_v41.rs, module doc, step 4, and engram_v41/apply.rs, `apply` (the
+ * `gate_k` launch over [tokens, hc] with streams, kv, qk, dim, hc, eps): a
+ * normalised dot of each stream against its key, a signed-sqrt sigmoid, and
+ * h += gate * value, in place on the fp32 streams [T, hc, dim].
+ * Readings (the pages give the words above and the arguments only):
+ *  - kv row t is [key_0 | ... | key_{hc-1} | value], dim values each: one key
+ *    per stream plus one shared value (engram_v41.rs module doc, "one key per
+ *    hyper-connection stream plus one shared value"), keys first;
+ *  - kv is the projection's output held as bf16 (the page's `kv` buffer is
+ *    bf16): every kv value is rounded to bf16 (fp32 RN, then bf16 RN) first;
+ *  - "normalised dot": the stream and the key are RMS-normalised with eps,
+ *    rms(z) = sqrt(mean(z^2) + eps), weighted by q_weight and k_weight (only
+ *    their product qk = q_weight * k_weight enters), and the dot is scaled by
+ *    1/sqrt(dim): s = sum_i qk_i h_i k_i / (rms(h) rms(k) sqrt(dim));
+ *  - "signed-sqrt sigmoid": g = 1 / (1 + exp(-sign(s) sqrt(|s|)));
+ *  - h_i += g * v_i for every i.
+ * fp64 throughout (the inputs are fp32 values). */
+void oracle_engram_gate(const float* streams, const float* kv, int64_t ld_kv, const float* qk, int64_t tokens,
+                        int64_t hc, int64_t dim, float eps, double* out, double* gates)
+{
+    for (int64_t t = 0; t < tokens; ++t) {
+        const float* v32 = kv + t * ld_kv + hc * dim;
+        for (int64_t c = 0; c < hc; ++c) {
+            const float* h = streams + (t * hc + c) * dim;
+            const float* k32 = kv + t * ld_kv + c * dim;
+            const float* q = qk + c * dim;
+            double shh = 0.0, skk = 0.0, shk = 0.0;
+            for (int64_t i = 0; i < dim; ++i) {
+                const double hv = h[i];
+                const double kk = oracle_bf16_to_double(oracle_f32_to_bf16(k32[i]));
+                shh += hv * hv;
+                skk += kk * kk;
+                shk += (double)q[i] * hv * kk;
+            }
+            const double rh = sqrt(shh / (double)dim + (double)eps);
+            const double rk = sqrt(skk / (double)dim + (double)eps);
+            const double s = shk / (rh * rk * sqrt((double)dim));
+            const double ss = s < 0.0 ? -sqrt(-s) : sqrt(s);
+            const double g = 1.0 / (1.0 + exp(-ss));
+            if (gates)
+                gates[t * hc + c] = g;
+            double* o = out + (t * hc + c) * dim;
+            for (int64_t i = 0; i < dim; ++i)
+                o[i] = (double)h[i] + g * oracle_bf16_to_double(oracle_f32_to_bf16(v32[i]));
+        }
+    }
+}
+
 int oracle_block_bytes(void) { return Q2K_BYTES; }
 int oracle_q3k_block_bytes(void) { return Q3K_BYTES; }
 int oracle_q8_1_block_bytes(void) { return Q8_1_BYTES; }

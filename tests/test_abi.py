@@ -32,7 +32,7 @@ def test_header_declares_the_boundary_calls():
     names = declared_functions()
     for want in ["q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16", "q2k_mmvq_q8_1", "q2k_mmvq_pair",
                  "q2k_mmvq_experts", "dense_gemm_bf16", "swiglu_q8_1_rows", "q2k_moe_m1", "q2k_mmvq_grouped",
-                 "q2k_engram_hash", "q3k_mmvq_q8_1", "q3k_mmvq_experts"]:
+                 "q2k_engram_hash", "q2k_engram_gate", "q3k_mmvq_q8_1", "q3k_mmvq_experts"]:
         assert want in names
 
 
@@ -180,3 +180,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         q.lib()
+
+
+def test_engram_gate_validation_before_any_launch(L):
+    import math
+    p = ctypes.c_void_p(0x10000)
+    G = lambda *a: L.q2k_engram_gate(*a)  # noqa: E731
+    # streams, kv, ld_kv, qk, tokens, hc, dim, eps, gates, stream
+    assert G(None, p, 20480, p, 1, 4, 4096, 1e-6, None, None) == 1
+    assert G(p, p, 20480, None, 1, 4, 4096, 1e-6, None, None) == 1
+    assert G(p, p, 20480, p, 1, 5, 4096, 1e-6, None, None) == 2     # hc in 1..4 (the page's limit)
+    assert G(p, p, 20480, p, 1, 0, 4096, 1e-6, None, None) == 2
+    assert G(p, p, 20479, p, 1, 4, 4096, 1e-6, None, None) == 2     # kv rows hold hc keys and the value
+    assert G(p, p, 20480, p, 1, 4, 0, 1e-6, None, None) == 2
+    assert G(p, p, 20480, p, -1, 4, 4096, 1e-6, None, None) == 2
+    assert G(p, p, 20480, p, 1, 4, 4096, -1.0, None, None) == 2
+    assert G(p, p, 20480, p, 1, 4, 4096, math.nan, None, None) == 2
+    assert G(ctypes.c_void_p(0x10002), p, 20480, p, 1, 4, 4096, 1e-6, None, None) == 3
+    assert G(p, p, 20480, p, 1, 4, 4096, 1e-6, ctypes.c_void_p(0x10001), None) == 3

@@ -249,3 +249,86 @@ def test_single_token_kernel_and_general_kernel_agree(lib):
     assert rel_err_rows(y_al, ref) <= TOL_BF16
     assert rel_err_rows(y_un, ref) <= TOL_BF16
     assert rel_err_rows(y_al, y_un) <= 1e-5
+
+
+# ---- the engram gate and the whole engram step -------------------------------------------
+
+@pytest.mark.parametrize("T,hc,dim,pad", [(1, 4, 4096, 0), (16, 4, 4096, 0), (3, 1, 1000, 5), (2, 2, 7, 0),
+                                          (5, 3, 2048, 64)])
+def test_engram_gate_against_oracle(lib, T, hc, dim, pad):
+    g = np.random.default_rng(T * 100 + hc * 10 + dim)
+    streams = g.standard_normal((T, hc, dim)).astype(np.float32)
+    # keys correlated with their streams so the gates spread over (0, 1)
+    kv = g.standard_normal((T, (hc + 1) * dim + pad)).astype(np.float32)
+    for c in range(hc):
+        kv[:, c * dim:(c + 1) * dim] += (g.uniform(-2, 2, (T, 1)) * streams[:, c, :]).astype(np.float32)
+    qk = g.uniform(0.5, 1.5, (hc, dim)).astype(np.float32)
+    ref, ref_g = oracle.engram_gate(streams, kv, qk, 1e-6)
+    sd = dev(streams)
+    gates = torch.empty((T, hc), dtype=torch.float32, device="cuda")
+    lib.q2k_engram_gate(sd, dev(kv), dev(qk), 1e-6, gates=gates)
+    got = sd.cpu().numpy().astype(np.float64)
+    for t in range(T):
+        for c in range(hc):
+            assert np.max(np.abs(got[t, c] - ref[t, c])) <= 1e-5 * np.linalg.norm(ref[t, c])
+    np.testing.assert_allclose(gates.cpu().numpy(), ref_g, rtol=0, atol=2e-6)
+    if T * hc > 4:
+        assert ref_g.min() < 0.4 and ref_g.max() > 0.6  # the gates did spread
+    # in place and deterministic: a second call on a fresh copy gives the same bits
+    sd2 = dev(streams)
+    lib.q2k_engram_gate(sd2, dev(kv), dev(qk), 1e-6)
+    assert torch.equal(sd2, sd)
+
+
+def _engram_tables(seed):
+    rng = np.random.default_rng(seed)
+    ng, nl, nh = 3, 2, 4
+    tm = rng.integers(0, 1 << 40, size=4096).astype(np.int64)
+    mults = rng.integers(-(1 << 62), 1 << 62, size=(nl, ng)).astype(np.int64)
+    primes = np.full((nl, ng - 1, nh), 131071, np.int64)
+    offsets = (np.arange(nl * (ng - 1) * nh, dtype=np.int64) % 8 * 65536).reshape(nl, (ng - 1) * nh)
+    return rng, dict(max_ngram=ng, n_layers=nl, n_heads=nh, multipliers=mults, primes=primes, offsets=offsets,
+                     pad_id=7), tm
+
+
+@pytest.mark.parametrize("T", [16, 1])
+def test_engram_step_hash_rows_projection_gate(lib, T):
+    """The whole engram step on the device (engram_v41.rs module doc, steps
+    1-4; engram_v41/apply.rs `apply`): hash -> one layer's row ids -> rows
+    -> projection (16 tokens: the bf16 GEMM over wkv; one token: the Q2_K
+    GEMV over wkv_q2k) -> gate on the fp32 streams [T, 4, 4096], against
+    the oracle's chain."""
+    dim, hc, cols, n_table, eps = 4096, 4, 8, 1 << 20, 1e-6
+    rng, args, tm = _engram_tables(40 + T)
+    toks = rng.integers(0, len(tm), size=T).astype(np.uint32)
+    ref_hash = oracle.engram_hash(tm, np.zeros(64, np.int64), toks, 0, **args)
+    ids_ref = oracle.layer_row_ids(ref_hash, 1).astype(np.int32)
+    table = synth.q2k_blocks(0, "cfg1.table", n_table)
+    streams = rng.standard_normal((T, hc, dim)).astype(np.float32)
+    qk = rng.uniform(0.5, 1.5, (hc, dim)).astype(np.float32)
+
+    hdev = lambda a: dev(np.asarray(a))  # noqa: E731
+    _, lid = lib.q2k_engram_hash(hdev(tm), torch.zeros(64, dtype=torch.int64, device="cuda"), hdev(toks), 0,
+                                 args["max_ngram"], args["n_layers"], args["n_heads"], hdev(args["multipliers"]),
+                                 hdev(args["primes"]), hdev(args["offsets"]), args["pad_id"], layer_index=1)
+    rows = lib.q2k_dequant_rows(dev(table), 256, ids=lid.view(-1))
+    ref_rows, bad = oracle.dequant_rows(table, n_table, 256, ids_ref, T * cols)
+    assert bad == 0
+    np.testing.assert_array_equal(host_bits(rows), ref_rows)
+    xr = oracle.bf16_to_f64(ref_rows.reshape(T, cols * 256))
+    if T > 1:
+        wkv = synth.bf16_normal(0, "cfg1.wkv", (dim * (hc + 1), cols * 256), std=0.02)
+        kv = lib.dense_gemm_bf16(rows.view(T, cols * 256), bf16_dev(wkv))
+        kv_ref = oracle.dense_gemm(ref_rows.reshape(T, cols * 256), wkv)
+    else:
+        wq = synth.q2k_matrix(0, "engram.wkv_q2k", dim * (hc + 1), cols * 256)
+        kv = lib.q2k_gemv_bf16(dev(wq), rows.view(1, cols * 256))
+        kv_ref = oracle_matvec(wq, dim * (hc + 1), cols * 256, xr)
+    assert rel_err_rows(kv.cpu().numpy(), kv_ref) <= TOL_BF16
+    sd = dev(streams)
+    lib.q2k_engram_gate(sd, kv, dev(qk), eps)
+    ref, _ = oracle.engram_gate(streams, kv_ref.astype(np.float32), qk, eps)
+    got = sd.cpu().numpy().astype(np.float64)
+    for t in range(T):
+        for c in range(hc):
+            assert np.max(np.abs(got[t, c] - ref[t, c])) <= TOL_BF16 * np.linalg.norm(ref[t, c])

@@ -698,3 +698,74 @@ def test_engram_rows_projection_order_and_orientation():
                                                                for w in oracle.decode_block(blk)])
     x = oracle.bf16_to_f64(rows.reshape(tokens, K))
     np.testing.assert_array_equal(y, x[:, perm])
+
+
+# ---- engram gate (engram_v41.rs module doc, step 4; engram_v41/apply.rs, the
+# `gate_k` launch): closed forms on built streams, keys and values ----------------
+
+def _sigmoid(z):
+    return 1.0 / (1.0 + math.exp(-z))
+
+
+def test_engram_gate_zero_qk_gives_half_gate_and_the_last_block_is_the_value():
+    T, hc, dim = 2, 3, 8
+    g = np.random.default_rng(3)
+    h = (g.integers(-64, 64, (T, hc, dim)) / 16.0).astype(np.float32)
+    kv = (g.integers(-64, 64, (T, (hc + 1) * dim)) / 8.0).astype(np.float32)  # bf16-exact values
+    out, gates = oracle.engram_gate(h, kv, np.zeros((hc, dim), np.float32), 1e-6)
+    np.testing.assert_array_equal(gates, np.full((T, hc), 0.5))
+    v = kv[:, hc * dim:].astype(np.float64)
+    np.testing.assert_array_equal(out, h.astype(np.float64) + 0.5 * v[:, None, :])
+
+
+def test_engram_gate_rounds_kv_to_bf16():
+    # values that bf16 rounds (1 + 2^-10 -> 1; 1 + 3*2^-9 -> 1 + 2^-7)
+    T, hc, dim = 1, 1, 4
+    h = np.zeros((T, hc, dim), np.float32)
+    kv = np.zeros((T, 2 * dim), np.float32)
+    kv[0, dim:] = [1 + 2.0 ** -10, 1 + 3 * 2.0 ** -9, -(1 + 2.0 ** -10), 2.0]
+    out, _ = oracle.engram_gate(h, kv, np.zeros((hc, dim), np.float32), 1e-6)  # zero stream: eps keeps rms > 0
+    np.testing.assert_array_equal(out[0, 0], 0.5 * np.array([1.0, 1 + 2.0 ** -7, -1.0, 2.0]))
+
+
+@pytest.mark.parametrize("dim", [16, 64])
+@pytest.mark.parametrize("a,b", [(2.0, 0.5), (-3.0, 1.0), (0.25, -4.0)])
+def test_engram_gate_parallel_stream_and_key(dim, a, b):
+    """h = a u, key = b u, qk = 1, eps = 0: the normalised dot is
+    sign(ab) sqrt(dim), so the gate is sigmoid(sign(ab) dim^(1/4))."""
+    u = (np.random.default_rng(dim).integers(1, 16, dim) * np.where(np.arange(dim) % 3 == 0, -1, 1)).astype(np.float64)
+    h = (a * u).astype(np.float32).reshape(1, 1, dim)
+    kv = np.concatenate([b * u, np.ones(dim)]).astype(np.float32).reshape(1, 2 * dim)  # bf16-exact
+    out, gates = oracle.engram_gate(h, kv, np.ones((1, dim), np.float32), 0.0)
+    want = _sigmoid(math.copysign(dim ** 0.25, a * b))
+    assert abs(gates[0, 0] - want) < 1e-14
+    np.testing.assert_allclose(out[0, 0], a * u + want, rtol=0, atol=1e-13)
+
+
+def test_engram_gate_eps_enters_each_rms():
+    dim, a, b, eps = 16, 0.5, 2.0, 0.75
+    u = np.ones(dim)
+    h = (a * u).astype(np.float32).reshape(1, 1, dim)
+    kv = np.concatenate([b * u, np.zeros(dim)]).astype(np.float32).reshape(1, 2 * dim)
+    _, gates = oracle.engram_gate(h, kv, np.ones((1, dim), np.float32), eps)
+    # mean(u^2) = 1: s = a b dim / (sqrt(a^2 + eps) sqrt(b^2 + eps) sqrt(dim))
+    s = a * b * math.sqrt(dim) / (math.sqrt(a * a + np.float32(eps)) * math.sqrt(b * b + np.float32(eps)))
+    assert abs(gates[0, 0] - _sigmoid(math.sqrt(s))) < 1e-14
+
+
+def test_engram_gate_each_stream_reads_its_own_key():
+    """Streams on disjoint supports with their own key equal to the stream:
+    each gate is sigmoid(dim^(1/4) * sqrt(...)) for its own key and exactly
+    0.5 had it read another stream's key (orthogonal, dot 0)."""
+    hc, dim = 4, 16
+    h = np.zeros((1, hc, dim), np.float32)
+    kv = np.zeros((1, (hc + 1) * dim), np.float32)
+    for c in range(hc):
+        h[0, c, 4 * c:4 * c + 4] = 1.0 + c
+        kv[0, c * dim + 4 * c:c * dim + 4 * c + 4] = 1.0
+    _, gates = oracle.engram_gate(h, kv, np.ones((hc, dim), np.float32), 0.0)
+    # mean(h^2) = (1+c)^2 / 4, mean(k^2) = 1/4, dot = 4 (1+c): s = 4 sqrt(dim) / dim * 4 = ...
+    for c in range(hc):
+        s = 4 * (1.0 + c) / (math.sqrt((1.0 + c) ** 2 / 4) * math.sqrt(1 / 4) * math.sqrt(dim))
+        assert abs(gates[0, c] - _sigmoid(math.sqrt(s))) < 1e-14
+        assert gates[0, c] > 0.5 + 1e-3
