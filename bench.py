@@ -650,6 +650,28 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         del Wds
         torch.cuda.empty_cache()
 
+    # m > 8: the Q2_K matmul on the tensor cores (weights expanded on-chip)
+    for Nn in (4096, 8192, 16384):
+        Wq = synth.q2k_matrix(0, f"sweep.W{Nn}x{Nn}", Nn, Nn)
+        R = copies_for(Wq.nbytes, l2)
+        Wqs = [torch.from_numpy(Wq).cuda() for _ in range(R)]
+        for m in (64, 256):
+            xx = torch.from_numpy(synth.bf16_normal(0, f"sweep.dense.x{m}.{Nn}", (m, Nn)).view(np.int16)).cuda()
+            yy = torch.empty((m, Nn), dtype=torch.float32, device="cuda")
+            el, n = graph_time(lambda i: check(L.q2k_mmq_bf16(P(Wqs[i % R]), Nn, Nn, P(xx), m, Nn, P(yy), Nn, cur()),
+                                               "mmq"), 200, 10)
+            flops = 2.0 * m * Nn * Nn
+            rec(f"q2k_mmq_bf16 m={m} N=K={Nn}", el / n, Wq.nbytes + 2 * m * Nn + 4 * m * Nn, m,
+                {"TFLOPs": flops / (el / n) / 1e12})
+            xq = q.q8_1_quantize_rows(xx.view(torch.bfloat16))
+            ws = torch.empty(q.q2k_mmq_q8_1_workspace_bytes(m, Nn), dtype=torch.uint8, device="cuda")
+            el, n = graph_time(lambda i: check(L.q2k_mmq_q8_1(P(Wqs[i % R]), Nn, Nn, P(xq), m, P(yy), Nn, P(ws),
+                                                              ws.numel(), cur()), "mmq8"), 200, 10)
+            rec(f"q2k_mmq_q8_1 m={m} N=K={Nn}", el / n, Wq.nbytes + xq.numel() + 4 * m * Nn, m,
+                {"TFLOPs": flops / (el / n) / 1e12, "launches_per_call": 2})
+        del Wqs
+        torch.cuda.empty_cache()
+
     if rank == 0 and all_out:
         with open(all_out, "w") as f:
             for d in out:

@@ -331,6 +331,37 @@ int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int64_t dim, i
                               const uint16_t* x_bf16, const float* route_w, float* y,
                               q2k_stream_t stream);
 
+/* Q2_K matmul for many tokens (moe_v41/init.rs, `MoeV41::new`: the
+ * `metrale_q2_k_mmq128_*` kernels with their q8_1 activation quantisers take
+ * the rows of more than 8 tokens; the prefill side of the path).
+ *   W   Q2_K [N, K], 16-byte aligned; K % 1024 == 0 (rows on 16-byte
+ *       boundaries, streamed four blocks at a time)
+ *   x   bf16 [m, K], row stride ldx (ldx % 8 == 0), 16-byte aligned
+ *   y   fp32 [m, N], row stride ldy: y = x W^T
+ * The weights are read as Q2_K (84 bytes per 256 weights) and expanded on
+ * the chip to bf16: each weight is d*sc*q - dmin*m in fp32 rounded once to
+ * bf16, the values q2k_dequant_rows gives; the products run on the tensor
+ * cores with fp32 accumulation.  So y equals dense_gemm_bf16(x, the
+ * dequantised W) up to the order of the fp32 sums.  Any m >= 1 (tokens in
+ * tiles of up to 256); for m <= 8 the GEMV/MMVQ calls read the weights
+ * once per call too and are the faster route.  When the library splits K
+ * across thread blocks (few weight tiles), partial sums are added with fp32
+ * atomics, so the last bits may differ between runs.
+ * Q2K_ERR_UNSUPPORTED when the driver offers no tensor-map encoder. */
+int q2k_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx, float* y,
+                 int64_t ldy, q2k_stream_t stream);
+
+/* Workspace bytes q2k_mmq_q8_1 needs: m * K * 2 (0 for a bad shape). */
+size_t q2k_mmq_q8_1_workspace_bytes(int64_t m, int64_t K);
+
+/* The Q2_K matmul over q8_1 activations: xq holds m q8_1 rows of K values
+ * (back to back).  The values they encode, f32(d) * q, are rounded once to
+ * bf16 into `workspace` (a launch of its own), then q2k_mmq_bf16 runs on
+ * them.  workspace: at least q2k_mmq_q8_1_workspace_bytes(m, K) bytes,
+ * 16-byte aligned.  Two launches. */
+int q2k_mmq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y, int64_t ldy,
+                 void* workspace, size_t workspace_bytes, q2k_stream_t stream);
+
 /* Dense bf16 GEMM on the tensor cores, any m >= 1 (engram_v41/apply.rs,
  * `ops::dense_gemm` for several tokens; moe_v41/init.rs `dense_gemm_bf16`).
  *   x bf16 [m, K], row stride ldx;  W bf16 [N, K] row-major;

@@ -28,6 +28,7 @@ EXPORTS = (
     "q3k_row_bytes", "q3k_mmvq_q8_1", "q3k_mmvq_experts",
     "swiglu_q8_1_rows",
     "q2k_moe_m1_workspace_bytes", "q2k_moe_m1", "q2k_moe_m1_static_scratch", "dense_gemm_bf16", "q2k_status_string",
+    "q2k_mmq_bf16", "q2k_mmq_q8_1_workspace_bytes", "q2k_mmq_q8_1",
     "q2k_last_cuda_error", "q2k_device_error",
 )
 
@@ -86,6 +87,9 @@ def lib() -> ctypes.CDLL:
             "q2k_moe_m1": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
             "q2k_moe_m1_static_scratch": (I32, [P, I64, I64, I64, P, P, P, P]),
             "dense_gemm_bf16": (I32, [P, I64, I64, I64, P, I64, P, I64, P]),
+            "q2k_mmq_bf16": (I32, [P, I64, I64, P, I64, I64, P, I64, P]),
+            "q2k_mmq_q8_1_workspace_bytes": (SZ, [I64, I64]),
+            "q2k_mmq_q8_1": (I32, [P, I64, I64, P, I64, P, I64, P, SZ, P]),
             "q2k_status_string": (ctypes.c_char_p, [I32]),
             "q2k_last_cuda_error": (I32, []),
             "q2k_device_error": (I32, [ctypes.POINTER(ctypes.c_int32), I32]),
@@ -330,6 +334,38 @@ def q2k_moe_m1_static_scratch(ptrs, E, dim, inter, x, route_w, y=None, stream=No
     _call("q2k_moe_m1_static_scratch", _ptr(ptrs), E, dim, inter, _ptr(x), _ptr(route_w), _ptr(y),
           _stream(stream))
     return y
+
+
+def q2k_mmq_q8_1_workspace_bytes(m, K) -> int:
+    return lib().q2k_mmq_q8_1_workspace_bytes(m, K)
+
+
+def q2k_mmq_bf16(W, x, out=None, stream=None):
+    """Q2_K ``[N, K]`` times bf16 ``x [m, K]`` for many tokens (the tensor
+    cores over the on-chip bf16 expansion) -> fp32 ``[m, N]``."""
+    _need_cuda(W, x, out)
+    m, K = x.shape
+    N = W.numel() // q2k_row_bytes(K)
+    if out is None:
+        out = torch.empty((m, N), dtype=torch.float32, device=x.device)
+    _call("q2k_mmq_bf16", _ptr(W), N, K, _ptr(x), m, x.stride(0), _ptr(out), out.stride(0), _stream(stream))
+    return out
+
+
+def q2k_mmq_q8_1(W, xq, K, out=None, workspace=None, stream=None):
+    """Q2_K ``[N, K]`` times q8_1 ``xq [m, K/32*36]`` for many tokens ->
+    fp32 ``[m, N]`` (the q8_1 values go through a bf16 workspace)."""
+    _need_cuda(W, xq, out, workspace)
+    m = xq.shape[0]
+    N = W.numel() // q2k_row_bytes(K)
+    if out is None:
+        out = torch.empty((m, N), dtype=torch.float32, device=xq.device)
+    need = lib().q2k_mmq_q8_1_workspace_bytes(m, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=xq.device)
+    _call("q2k_mmq_q8_1", _ptr(W), N, K, _ptr(xq), m, _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
+          _stream(stream))
+    return out
 
 
 def dense_gemm_bf16(x, W, out=None, stream=None):

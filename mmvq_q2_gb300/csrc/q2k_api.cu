@@ -126,10 +126,12 @@ int q2k_device_error(int32_t* host_out, int clear)
 {
     if (!host_out)
         return Q2K_ERR_NULL_ARG;
-    int32_t a = 0, b = 0, c = 0, d = 0, q = 0, o = 0;
+    int32_t a = 0, b = 0, c = 0, d = 0, q = 0, o = 0, mq = 0;
     cudaError_t e = mv_error_word(&a, clear != 0);
     if (e == cudaSuccess)
         e = m1_error_word(&o, clear != 0);
+    if (e == cudaSuccess)
+        e = mmq_error_word(&mq, clear != 0);
     if (e == cudaSuccess)
         e = gemm_error_word(&b, clear != 0);
     if (e == cudaSuccess)
@@ -140,7 +142,7 @@ int q2k_device_error(int32_t* host_out, int clear)
         e = q3_error_word(&q, clear != 0);
     if (e != cudaSuccess)
         return fail_cuda(e);
-    *host_out = a | b | c | d | q | o;
+    *host_out = a | b | c | d | q | o | mq;
     return Q2K_OK;
 }
 
@@ -577,6 +579,55 @@ int q2k_moe_m1(const void* const* ptrs, int64_t E, int64_t dim, int64_t inter, c
     if ((e = launch_mv(d, s)) != cudaSuccess)
         return fail_cuda(e);
     return finish(launch_expert_sum(down_out, route_w, E, dim, y, s));
+}
+
+size_t q2k_mmq_q8_1_workspace_bytes(int64_t m, int64_t K)
+{
+    if (m < 1 || m > (1 << 24) || K <= 0 || K % 1024 || K > kMaxK)
+        return 0;
+    return mmq_q8_1_workspace(m, K);
+}
+
+int q2k_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx, float* y,
+                 int64_t ldy, q2k_stream_t stream)
+{
+    if (!W || !x || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (N < 1 || N > (1 << 30) || K <= 0 || K % 1024 || K > kMaxK || m < 1 || m > (1 << 24) || ldx < K || ldx % 8 ||
+        ldy < N)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (!mmq_supported(m, N, K))
+        return Q2K_ERR_UNSUPPORTED;  // no tensor-map encoder in this driver
+    return finish(launch_mmq_bf16(W, N, K, x, m, ldx, y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q2k_mmq_q8_1(const void* W, int64_t N, int64_t K, const void* xq, int64_t m, float* y, int64_t ldy,
+                 void* workspace, size_t workspace_bytes, q2k_stream_t stream)
+{
+    if (!W || !xq || !y)
+        return Q2K_ERR_NULL_ARG;
+    if (N < 1 || N > (1 << 30) || K <= 0 || K % 1024 || K > kMaxK || m < 1 || m > (1 << 24) || ldy < N)
+        return Q2K_ERR_BAD_SHAPE;
+    if (!workspace || workspace_bytes < q2k_mmq_q8_1_workspace_bytes(m, K))
+        return Q2K_ERR_WORKSPACE;
+    if (!aligned(W, 16) || !aligned(xq, 4) || !aligned(y, 4) || !aligned(workspace, 16))
+        return Q2K_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != Q2K_OK)
+        return st;
+    if (!mmq_supported(m, N, K))
+        return Q2K_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* xb = static_cast<uint16_t*>(workspace);
+    cudaError_t e = launch_q8_1_to_bf16(xq, m, K, xb, s);
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    return finish(launch_mmq_bf16(W, N, K, xb, m, K, y, ldy, s));
 }
 
 int dense_gemm_bf16(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W, int64_t N, float* y,

@@ -90,6 +90,16 @@ bool umma_supported(int64_t m, int64_t K, int64_t N);
 cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_t ldx, const uint16_t* W,
                                  int64_t N, float* y, int64_t ldy, cudaStream_t s);
 
+// Q2_K matmul for many tokens on tcgen05 (q2k_mmq.cu): y = x W^T with the
+// weights expanded from Q2_K to bf16 on-chip.  K % 1024 == 0, W and x
+// 16-byte aligned, ldx % 8 == 0.
+bool mmq_supported(int64_t m, int64_t N, int64_t K);
+cudaError_t launch_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx, float* y,
+                            int64_t ldy, cudaStream_t s);
+// q8_1 rows -> bf16 rows of the values they encode (rounded once to bf16).
+cudaError_t launch_q8_1_to_bf16(const void* xq, int64_t m, int64_t K, uint16_t* out, cudaStream_t s);
+size_t mmq_q8_1_workspace(int64_t m, int64_t K);
+
 // Q3_K MMVQ with q8_1 activations (m = 1..8): one matrix, or n_seg matrices
 // from W_table (N rows each, y row block e at y + e * y_seg_stride).
 struct Q3Problem {
@@ -110,6 +120,7 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s);
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
 cudaError_t m1_error_word(int32_t* out, bool clear);
+cudaError_t mmq_error_word(int32_t* out, bool clear);
 cudaError_t gemm_error_word(int32_t* out, bool clear);
 cudaError_t mt_error_word(int32_t* out, bool clear);
 cudaError_t umma_error_word(int32_t* out, bool clear);

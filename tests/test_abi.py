@@ -32,7 +32,8 @@ def test_header_declares_the_boundary_calls():
     names = declared_functions()
     for want in ["q2k_dequant_rows", "q8_1_quantize_rows", "q2k_gemv_bf16", "q2k_mmvq_q8_1", "q2k_mmvq_pair",
                  "q2k_mmvq_experts", "dense_gemm_bf16", "swiglu_q8_1_rows", "q2k_moe_m1", "q2k_mmvq_grouped",
-                 "q2k_engram_hash", "q2k_engram_gate", "q3k_mmvq_q8_1", "q3k_mmvq_experts"]:
+                 "q2k_engram_hash", "q2k_engram_gate", "q3k_mmvq_q8_1", "q3k_mmvq_experts", "q2k_mmq_bf16",
+                 "q2k_mmq_q8_1"]:
         assert want in names
 
 
@@ -198,3 +199,20 @@ def test_engram_gate_validation_before_any_launch(L):
     assert G(p, p, 20480, p, 1, 4, 4096, math.nan, None, None) == 2
     assert G(ctypes.c_void_p(0x10002), p, 20480, p, 1, 4, 4096, 1e-6, None, None) == 3
     assert G(p, p, 20480, p, 1, 4, 4096, 1e-6, ctypes.c_void_p(0x10001), None) == 3
+
+
+def test_mmq_validation_before_any_launch(L):
+    p16 = ctypes.c_void_p(0x10000)
+    # W, N, K, x, m, ldx, y, ldy, stream
+    assert L.q2k_mmq_bf16(None, 64, 4096, p16, 64, 4096, p16, 64, None) == 1
+    assert L.q2k_mmq_bf16(p16, 64, 4352, p16, 64, 4352, p16, 64, None) == 2   # K % 1024
+    assert L.q2k_mmq_bf16(p16, 64, 4096, p16, 0, 4096, p16, 64, None) == 2
+    assert L.q2k_mmq_bf16(p16, 64, 4096, p16, 64, 4100, p16, 64, None) == 2   # ldx % 8
+    assert L.q2k_mmq_bf16(p16, 64, 4096, p16, 64, 4096, p16, 63, None) == 2
+    assert L.q2k_mmq_bf16(ctypes.c_void_p(0x10004), 64, 4096, p16, 64, 4096, p16, 64, None) == 3
+    assert L.q2k_mmq_bf16(p16, 64, 4096, ctypes.c_void_p(0x10008), 64, 4096, p16, 64, None) == 3
+    assert L.q2k_mmq_q8_1_workspace_bytes(64, 4096) == 64 * 4096 * 2
+    assert L.q2k_mmq_q8_1_workspace_bytes(64, 4352) == 0
+    need = L.q2k_mmq_q8_1_workspace_bytes(64, 4096)
+    assert L.q2k_mmq_q8_1(p16, 64, 4096, p16, 64, p16, 64, p16, need - 1, None) == 6
+    assert L.q2k_mmq_q8_1(p16, 64, 4096, p16, 64, p16, 64, None, need, None) == 6
