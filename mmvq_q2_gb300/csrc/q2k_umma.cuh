@@ -1,8 +1,8 @@
 // tcgen05 / TMA building blocks shared by the dense bf16 GEMM (q2k_umma.cu)
 // and the Q2_K matmul for many tokens (q2k_mmq.cu): 2-D tensor copies, the
 // shared-memory matrix descriptor of a 128-byte-swizzled K-major tile, the
-// kind::f16 MMA with its instruction descriptor, commit, and the tensor
-// memory load of the epilogue.  sm_103a only.
+// kind::f16 MMA (A from shared or tensor memory) with its instruction
+// descriptor, commit, and tensor memory loads and stores.  sm_103a only.
 #pragma once
 
 #include <cuda.h>
@@ -56,6 +56,34 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
         : "memory");
 }
+
+// The same MMA with A read from tensor memory: lane r holds row r of the
+// 128-row operand, and 32-bit column c holds K = 2c (low half) and 2c + 1.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                bool acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one register
+// per column per lane); tcgen05.wait::st makes them complete.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {

@@ -68,6 +68,23 @@ def test_mmq_bf16_against_oracle_and_the_dense_gemm_of_the_expansion(lib, m, N, 
     assert rel_err_rows(y, yd) <= 1e-5
 
 
+@pytest.mark.parametrize("m,N,K", [(20, 51200, 1024), (140, 20000, 1024), (48, 30000, 3072)])
+def test_mmq_many_pieces_per_cta(lib, m, N, K):
+    """More (tile, 1024-K) units than SMs: CTAs finish several tiles in turn,
+    so the accumulators are reused (two of them up to 128 tokens, one
+    above) and tiles straddle CTAs.  Every row against the dense GEMM of the
+    expansion, sampled rows (two per 128-row tile) against the oracle."""
+    W = synth.q2k_matrix(23, f"mmq.pieces.W.{N}.{K}", N, K)
+    x = synth.bf16_normal(23, f"mmq.pieces.x.{m}.{K}", (m, K))
+    Wd, xd = dev(W), bf16_dev(x)
+    y = lib.q2k_mmq_bf16(Wd, xd).cpu().numpy()
+    yd = lib.dense_gemm_bf16(xd, lib.q2k_dequant_rows(Wd, K)).cpu().numpy()
+    assert rel_err_rows(y, yd) <= 1e-5
+    rows = np.unique(np.concatenate([np.arange(0, N, 128), np.minimum(np.arange(127, N + 127, 128), N - 1)]))
+    ref = oracle.matvec(np.ascontiguousarray(W.reshape(N, -1)[rows]), len(rows), K, x_f64(x))
+    assert rel_err_rows(y[:, rows], ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("m,N,K", [(9, 300, 2048), (64, 1024, 4096), (256, 384, 2048)])
 def test_mmq_q8_1_against_oracle(lib, m, N, K):
     W = synth.q2k_matrix(21, f"mmq8.W.{N}.{K}", N, K)
