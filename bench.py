@@ -19,12 +19,13 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   on every host core (threads over output rows; the line's value).
 * --impl reference times the CPU oracle on the same workload on every host
   core (rank 0 only).
-* --ncu-case [mv|mt|gemm|small|q3k] runs a few untimed calls for a profiler
+* --ncu-case [mv|mt|gemm|small|q3k|mmq] runs a few untimed calls for a profiler
   capture and prints no JSON line: mv = the headline kernel (bf16 GEMV) and
   the q8_1 MMVQ at m=1 on the headline shape; mt = the same shape at m=8
   (the tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
   N=K=16384; small = one call of every other kernel at the configurations'
-  shapes.
+  shapes; q3k = the Q3_K MMVQ at m=1 and 2; mmq = the Q2_K matmul for many
+  tokens at m=64 and m=256, N=K=16384.
 * --all also times every configuration of the sweep and prints one JSON
   object per configuration to stderr (and to the file --all-out names).
 With torchrun (N > 1) every rank runs an independent replica (the path is
@@ -765,7 +766,8 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     weights).  mt: the same at m=8.  gemm: dense_gemm_bf16 at m=64, then
     m=256, N=K=16384 (537 MB of bf16 weights), one call each.  q3k:
     `calls` calls of q3k_mmvq_q8_1 at m=1, then at m=2, N=K=16384 (115 MB of
-    Q3_K weights)."""
+    Q3_K weights).  mmq: q2k_mmq_bf16 at m=64, then m=256, N=K=16384 (88 MB
+    of Q2_K weights), one call each."""
     import torch
     from mmvq_q2_gb300 import build as b
     b.build()
@@ -783,6 +785,15 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
             xq = q.q8_1_quantize_rows(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
             for _ in range(calls):
                 q.q3k_mmvq_q8_1(Wd, xq, K_HEAD)
+        torch.cuda.synchronize()
+        print("ncu case done", file=sys.stderr)
+        return
+    if which == "mmq":
+        W = synth.q2k_matrix(0, "sweep.W16384", N_HEAD, K_HEAD)
+        Wd = torch.from_numpy(W).cuda()
+        for m in (64, 256):
+            x = synth.bf16_normal(0, f"sweep.dense.x{m}", (m, K_HEAD))
+            q.q2k_mmq_bf16(Wd, torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
         torch.cuda.synchronize()
         print("ncu case done", file=sys.stderr)
         return
@@ -816,7 +827,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
     ap.add_argument("--all-out", default=None, help="also write the --all records here, one JSON object a line")
-    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k"], default=None)
+    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k", "mmq"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
