@@ -1,15 +1,19 @@
-// Q2_K GEMV / MMVQ for one token over long rows (engram_v41/apply.rs, the
-// single-token `engram_v41_wkv_q2k_gemv` off `wkv_q2k`; attn_v41/decode.rs,
-// `kquant_mmvq_pair_w` for the pair at m = 1).
+// Q2_K GEMV / MMVQ for one, two or four tokens over long rows
+// (engram_v41/apply.rs, the single-token `engram_v41_wkv_q2k_gemv` off
+// `wkv_q2k`; attn_v41/decode.rs, `kquant_mmvq_pair_w` for the pair; the
+// m <= 8 MMVQ of moe_v41/init.rs).
 //
 // One CTA of 16 warps per SM owns a contiguous range of output rows.  The
 // CTA's lanes are split into row teams: a team has one lane per half block
-// of a row (2*K/256 lanes, rounded up to a power of two), so each lane owns
-// a fixed 128-weight slice of every row and keeps the matching activations
-// in registers (q2k_slice.cuh).
+// of a row for one token (8-word slices: 2*K/256 lanes, rounded up to a
+// power of two), or per quarter block for two or four tokens (4-word
+// slices, 4*K/256 lanes: the same registers for the activations), so each
+// lane owns a fixed slice of every row and keeps the matching activations
+// of every token in registers (q2k_slice.cuh).
 //
-// Weight stream.  A stage is two rows per team: 2T consecutive rows of the
-// CTA's range (about 43 KB), so it arrives with a single 1-D bulk copy.  The
+// Weight stream.  A stage is 16/SW rows per team (two rows with 8-word
+// slices, four with 4-word ones): about 43 KB of consecutive rows of the
+// CTA's range, so it arrives with a single 1-D bulk copy.  The
 // copy size is what sets the stream rate on this part: rings of 1.3 KB or
 // 5 KB copies stream the 16384^2 matrix at 3.6 and 4.3 TB/s, 21 KB and
 // 43 KB copies at 6.3 and 6.4 TB/s (plain 16-byte loads: 6.15).  Two rows
@@ -46,12 +50,15 @@ namespace {
 
 constexpr int kM1Threads = 512;  // 16 warps of row teams
 constexpr int kM1Warps = kM1Threads / 32;
-constexpr int kM1Rpt = 4;  // rows per lane between two reductions
-constexpr int kM1Rps = 2;  // rows per team in a stage
+// rows per team in a stage: a stage of about 43 KB whatever the slice width
+__host__ __device__ constexpr int m1_rps(int sw) { return 16 / sw; }
+// rows per lane between two reductions: at least 4, and whole stages
+__host__ __device__ constexpr int m1_rpt(int sw) { return m1_rps(sw) > 4 ? m1_rps(sw) : 4; }
 
 struct M1Args {
     const uint8_t* W[2];  // row space: rows [0, N0) of W[0], then rows of W[1]
     float* y[2];
+    int64_t ldy[2];       // floats between tokens of y
     int N0;
     int rows_total;
     int rows_q, rows_r;  // CTA c owns rows_q rows (+1 if c < rows_r)
@@ -63,8 +70,9 @@ struct M1Args {
     int depth;           // stages in the ring
     uint32_t row_bytes;  // nb * 84, a multiple of 16
     uint32_t stage_bytes;  // kM1Rps * teams * row_bytes
-    const uint8_t* x;    // bf16 row or q8_1 row
-    uint32_t x_bytes;
+    const uint8_t* x;    // bf16 rows or q8_1 rows, one per token
+    int64_t x_tok_stride;  // bytes between tokens (a multiple of 16)
+    uint32_t x_bytes;    // bytes of one token's row
     uint32_t off_x, off_bar, off_red;
 };
 
@@ -74,11 +82,15 @@ __device__ __forceinline__ void m1_flag_error(volatile int* abort_flag)
     *abort_flag = 1;
 }
 
-template <int ACT>
+template <int ACT, int M, int SW>
 __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    using S = Slice<1, ACT, 8>;
+    using S = Slice<M, ACT, SW>;
+    constexpr int kM1Rps = m1_rps(SW);
+    constexpr int kM1Rpt = m1_rpt(SW);
+    constexpr int VP = kM1Rpt * M;  // values per lane between two reductions
+    static_assert(VP <= 32, "one (row, token) value per lane at most");
     pdl_launch_dependents();  // the next kernel may set itself up meanwhile
 
     const int tid = threadIdx.x;
@@ -139,8 +151,11 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
     if (tid == 0) {
         // the activations first (every CTA reads them: keep them in L2), then
         // the whole ring, before any arithmetic
-        mbar_arrive_expect_tx(smem_u32(xbar), a.x_bytes);
-        bulk_copy_g2s_hint(smem_u32(xsm), a.x, a.x_bytes, smem_u32(xbar), l2_policy_evict_last());
+        mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)M * a.x_bytes);
+#pragma unroll
+        for (int t = 0; t < M; ++t)
+            bulk_copy_g2s_hint(smem_u32(xsm + (size_t)t * a.x_bytes), a.x + (int64_t)t * a.x_tok_stride, a.x_bytes,
+                               smem_u32(xbar), l2_policy_evict_last());
         for (int j = 0; j < min(a.depth, nst); ++j)
             issue(j, j);
     }
@@ -157,17 +172,22 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
         return false;
     };
 
-    // ---- this lane's activation slice ----
-    const bool active = li < 2 * a.nb;
-    const int b = active ? li >> 1 : 0;  // block within the row
-    const int n = li & 1;                // half block
+    // ---- this lane's activation slice: block b, half n, first qs word wi0 ----
+    constexpr int kLanesPerBlock = 16 / SW;  // 2, 4 or 8 (2 halves x 8/SW slices)
+    const bool active = li < kLanesPerBlock * a.nb;
+    const int b = active ? li / kLanesPerBlock : 0;
+    const int n = (li / (kLanesPerBlock / 2)) & 1;
+    const int wi0 = SW * (li & (kLanesPerBlock / 2 - 1));
     S sl;
     bool aborted = !wait(smem_u32(xbar), 0);
-    if constexpr (ACT == ACT_BF16)
-        convert_x_bf16<1, 8>(xsm, a.nb);  // every thread (two CTA barriers inside)
+    // bf16 rows of one or two tokens are converted in place, cooperatively
+    // (their region is sized for it); four tokens convert per thread inside
+    // load_slice, from the raw rows
+    if constexpr (coop_x<M, ACT, SW>())
+        convert_x_bf16<M, SW>(xsm, a.nb);  // every thread (two CTA barriers inside)
 
     {
-        load_slice<1, ACT, 8>(sl, xsm, a.nb, b, n, 0, active);
+        load_slice<M, ACT, SW>(sl, xsm, a.nb, b, n, wi0, active);
 
         const uint8_t* blk0 = ring + (size_t)team * kM1Rps * a.row_bytes + (size_t)b * kBlockBytes;
         // stage j's slot, the parity of its phase there, j / depth and this
@@ -186,12 +206,15 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
                 aborted = true;
 #pragma unroll
             for (int q = 0; q < kM1Rps; ++q) {
-                v[q] = 0.f;
-                if (!aborted && (!tail || row + q < hi)) {
-                    float acc[1] = {0.f};
-                    slice_dot<1, ACT, 8>(sl, blk0 + (size_t)s * a.stage_bytes + (size_t)q * a.row_bytes, n, 0, acc);
-                    v[q] = acc[0];
-                }
+                float acc[M];
+#pragma unroll
+                for (int t = 0; t < M; ++t)
+                    acc[t] = 0.f;
+                if (!aborted && (!tail || row + q < hi))
+                    slice_dot<M, ACT, SW>(sl, blk0 + (size_t)s * a.stage_bytes + (size_t)q * a.row_bytes, n, wi0, acc);
+#pragma unroll
+                for (int t = 0; t < M; ++t)
+                    v[q * M + t] = acc[t];
             }
             __syncwarp();
             if (lane == 0) {
@@ -211,35 +234,38 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
                 ++kd;
             }
         };
-        // value k of v is row Rps*t + (k % Rps) of stage j0 + k / Rps; each
-        // lane group of 8 ends up with one row's warp partial
+        // value i = k*M + t of v is token t of row Rps*team + (k % Rps) of
+        // stage j0 + k / Rps; each lane group of 32/VP ends up with one
+        // (row, token) warp partial
         constexpr int SPG = kM1Rpt / kM1Rps;  // stages per reduction group
-        auto deposit = [&](int j0, float (&v)[kM1Rpt]) {
-            const float r = transpose_reduce<kM1Rpt>(v, lane);
-            const int k = lane >> 3;
+        constexpr int kGroupLanes = 32 / VP;
+        auto deposit = [&](int j0, float (&v)[VP]) {
+            const float r = transpose_reduce<VP>(v, lane);
+            const int i = lane / kGroupLanes;
+            const int k = i / M, t = i - k * M;
             const int rl = spr * (j0 + k / kM1Rps) + kM1Rps * team + k % kM1Rps;  // row within the CTA's range
-            if ((lane & 7) == 0 && lo + rl < hi)
-                red[(size_t)rl * a.wpt + wit] = r;
+            if ((lane & (kGroupLanes - 1)) == 0 && lo + rl < hi)
+                red[((size_t)rl * M + t) * a.wpt + wit] = r;
         };
         const int nst_full = (hi - lo) / spr;  // stages with every row present
         int j0 = 0;
         for (; j0 + SPG <= nst_full; j0 += SPG) {
-            float v[kM1Rpt];
+            float v[VP];
 #pragma unroll
             for (int g = 0; g < SPG; ++g)
-                stage(j0 + g, false, v + g * kM1Rps);
+                stage(j0 + g, false, v + g * kM1Rps * M);
             deposit(j0, v);
         }
         for (; j0 < nst; j0 += SPG) {
-            float v[kM1Rpt];
+            float v[VP];
 #pragma unroll
             for (int g = 0; g < SPG; ++g) {
                 if (j0 + g < nst) {
-                    stage(j0 + g, true, v + g * kM1Rps);
+                    stage(j0 + g, true, v + g * kM1Rps * M);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < kM1Rps; ++q)
-                        v[g * kM1Rps + q] = 0.f;
+                    for (int q = 0; q < kM1Rps * M; ++q)
+                        v[g * kM1Rps * M + q] = 0.f;
                 }
             }
             deposit(j0, v);
@@ -258,16 +284,17 @@ __global__ void __launch_bounds__(kM1Threads, 1) q2k_m1_kernel(const M1Args a)
         __syncthreads();
         return;
     }
-    // the warps' partials of each row, added in warp order
-    for (int r = tid; r < hi - lo; r += blockDim.x) {
+    // the warps' partials of each (row, token), added in warp order
+    for (int i = tid; i < (hi - lo) * M; i += blockDim.x) {
+        const int r = i / M, t = i - r * M;
         float v = 0.f;
         for (int w = 0; w < a.wpt; ++w)
-            v += red[(size_t)r * a.wpt + w];
+            v += red[(size_t)i * a.wpt + w];
         const int row = lo + r;
         if (row < a.N0)
-            a.y[0][row] = v;
+            a.y[0][(int64_t)t * a.ldy[0] + row] = v;
         else
-            a.y[1][row - a.N0] = v;
+            a.y[1][(int64_t)t * a.ldy[1] + row - a.N0] = v;
     }
 }
 
@@ -284,36 +311,49 @@ int log2i(int v)
 // The launch plan; false when the problem is not this kernel's.
 bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, size_t& smem)
 {
-    if (p.m != 1 || p.W_table || p.w_seg_stride || p.x_prep || p.n_seg < 1 || p.n_seg > 2)
+    // one token (8-word slices), two or four (4-word slices; four only with
+    // q8_1: four bf16 tokens in 2-word slices were slower here than the
+    // tensor-core kernel, 22.8 vs 20.2 us at 8192^2)
+    const bool tokens_ok = p.m == 1 || p.m == 2 || (p.m == 4 && p.act == ACT_Q8);
+    if (!tokens_ok || p.W_table || p.w_seg_stride || p.x_prep || p.n_seg < 1 || p.n_seg > 2)
         return false;
-    // Rows of 32..128 blocks: the rows the general kernel also walks with
-    // 128-weight slices, so the two give the same bits (the pair from bf16
-    // and the expert batches run there and promise equality with this one)
+    // Rows of 32..128 blocks: for one token, the rows the general kernel
+    // also walks with 128-weight slices, so the two give the same bits (the
+    // pair from bf16 and the expert batches run there and promise equality
+    // with this one)
     if (p.K % 1024 || p.K < 32 * kBlockWeights || p.K > 128 * kBlockWeights)
         return false;
     const int nseg = p.n_seg;
     for (int e = 0; e < nseg; ++e)
         if ((reinterpret_cast<uintptr_t>(p.W[e]) & 15u) || p.N[e] <= 0)
             return false;
-    if (reinterpret_cast<uintptr_t>(p.x) & 15u)
+    if ((reinterpret_cast<uintptr_t>(p.x) & 15u) || (p.m > 1 && (p.x_tok_stride & 15)))
         return false;
     const int64_t rows = p.N[0] + (nseg > 1 ? p.N[1] : 0);
     if (rows > (1 << 30))
         return false;
+    const int sw = p.m == 1 ? 8 : 4;
+    // bf16 activations of one or two tokens are converted cooperatively:
+    // every 16-value group of every token needs a thread slot
+    if (p.act == ACT_BF16 && p.m <= 2 && p.m * (p.K / 16) > kCoopGroupsPerThread * kM1Threads)
+        return false;
     a = M1Args{};
     a.nb = (int)(p.K / kBlockWeights);
-    a.lanes = std::max(32, 1 << log2i(2 * a.nb));
+    a.lanes = std::max(32, 1 << log2i((16 / sw) * a.nb));
     if (a.lanes > kM1Threads)
         return false;
     a.log_lanes = log2i(a.lanes);
     a.teams = kM1Threads / a.lanes;
     a.wpt = a.lanes / 32;
     a.row_bytes = (uint32_t)(a.nb * kBlockBytes);
-    a.stage_bytes = (uint32_t)(kM1Rps * a.teams) * a.row_bytes;
+    a.stage_bytes = (uint32_t)(m1_rps(sw) * a.teams) * a.row_bytes;
     a.W[0] = static_cast<const uint8_t*>(p.W[0]);
     a.W[1] = static_cast<const uint8_t*>(nseg > 1 ? p.W[1] : p.W[0]);
     a.y[0] = p.y[0];
     a.y[1] = nseg > 1 ? p.y[1] : p.y[0];
+    a.ldy[0] = p.ldy[0];
+    a.ldy[1] = nseg > 1 ? p.ldy[1] : p.ldy[0];
+    a.x_tok_stride = p.x_tok_stride;
     a.N0 = (int)p.N[0];
     a.rows_total = (int)rows;
     a.x = static_cast<const uint8_t*>(p.x);
@@ -322,7 +362,8 @@ bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, siz
     a.rows_q = (int)(rows / grid);
     a.rows_r = (int)(rows % grid);
     const int rows_cta = a.rows_q + (a.rows_r ? 1 : 0);
-    const size_t x_region = p.act == ACT_BF16 ? align16((size_t)coop_x_bytes(1, a.nb)) : align16(a.x_bytes);
+    const size_t x_region = p.act == ACT_BF16 && p.m <= 2 ? align16((size_t)coop_x_bytes(p.m, a.nb))
+                                                           : align16((size_t)p.m * a.x_bytes);
     const size_t cap = std::min<size_t>((size_t)di.smem_optin, 227 * 1024);
     for (int depth = 8; depth >= 2; --depth) {
         a.depth = depth;
@@ -330,18 +371,18 @@ bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, siz
         a.off_bar = (uint32_t)(a.off_x + x_region);
         a.off_red = (uint32_t)align16(a.off_bar + (size_t)(depth + 2) * sizeof(uint64_t) +
                                       (size_t)(2 * depth) * sizeof(int));
-        const int spr = kM1Rps * a.teams;
-        smem = align16(a.off_red + (size_t)spr * ((rows_cta + spr - 1) / spr) * a.wpt * sizeof(float));
+        const int spr = m1_rps(sw) * a.teams;
+        smem = align16(a.off_red + (size_t)spr * ((rows_cta + spr - 1) / spr) * p.m * a.wpt * sizeof(float));
         if (smem <= cap)
             return true;
     }
     return false;
 }
 
-template <int ACT>
+template <int ACT, int M, int SW>
 cudaError_t launch_m1_act(const M1Args& a, int grid, size_t smem, cudaStream_t s)
 {
-    auto k = q2k_m1_kernel<ACT>;
+    auto k = q2k_m1_kernel<ACT, M, SW>;
     static int configured_for = -1;
     static size_t configured_smem = 0;
     int dev = 0;
@@ -382,7 +423,11 @@ cudaError_t launch_m1(const MvProblem& p, cudaStream_t s)
     size_t smem;
     if (!plan_m1(p, di, a, grid, smem))
         return cudaErrorInvalidValue;
-    return p.act == ACT_BF16 ? launch_m1_act<ACT_BF16>(a, grid, smem, s) : launch_m1_act<ACT_Q8>(a, grid, smem, s);
+    if (p.act == ACT_BF16)
+        return p.m == 1 ? launch_m1_act<ACT_BF16, 1, 8>(a, grid, smem, s) : launch_m1_act<ACT_BF16, 2, 4>(a, grid, smem, s);
+    if (p.m == 1)
+        return launch_m1_act<ACT_Q8, 1, 8>(a, grid, smem, s);
+    return p.m == 2 ? launch_m1_act<ACT_Q8, 2, 4>(a, grid, smem, s) : launch_m1_act<ACT_Q8, 4, 4>(a, grid, smem, s);
 }
 
 cudaError_t m1_error_word(int32_t* out, bool clear)
