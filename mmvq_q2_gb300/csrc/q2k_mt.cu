@@ -26,9 +26,12 @@
 //
 // Weights stream through a shared-memory ring of stages (a 16-row tile by a
 // K chunk of 16 blocks), each filled by one 2-D tensor copy (rows 16 bytes
-// aligned) that any warp may claim.  Warp w owns one block of the stage's tile.  The last warp to
-// finish a stage adds the 16 warps' partial sums in warp order into the
-// CTA's per-row accumulators, so results do not depend on timing.
+// aligned).  Warp w owns one block of every stage's tile and adds its
+// partial sums into accumulators of its own in shared memory (per row and
+// token), visiting the K chunks in order; after the walk the 16 warps'
+// accumulators of each output are added in warp order, so results do not
+// depend on timing or on which CTA holds a row.  The last warp out of a
+// stage refills its slot; waits sleep in the mbarrier (bounded).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -49,6 +52,7 @@ constexpr int kMtThreads = 512;
 constexpr int kMtWarps = kMtThreads / 32;
 constexpr int kTile = 16;  // weight rows per MMA tile (m16)
 constexpr int kTok = 8;    // tokens per MMA (n8)
+constexpr int kMtTilesPerCta = 8;  // bounds the warps' accumulators to 64 KB
 
 struct MtArgs {
     const uint8_t* W[2];
@@ -74,9 +78,8 @@ struct MtArgs {
     uint32_t stage_bytes;
     uint32_t rstride;      // bytes per row in a stage (nbc * 84)
     int w_aligned;         // every copied row piece is 16-byte aligned
-    int yacc_rows;
-    int ychunks;           // per-chunk accumulators (nchunks <= 8), else 1
-    uint32_t off_x, off_red, off_yacc, off_bar, off_cnt;
+    int yacc_rows;         // rows per warp accumulator: at most kMtTilesPerCta tiles
+    uint32_t off_x, off_yacc, off_bar, off_cnt;
 };
 
 struct Tile {
@@ -261,11 +264,11 @@ template <int ACT>
 __device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk1, const BOps& o, int cq,
                                          float (&part)[4])
 {
-    uint32_t sw0[4], sw1[4];  // scale bytes 0..15
+    uint32_t sw0[4], sw1[4];  // scale nibbles of sub-blocks 0..15, one per byte
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        sw0[q] = lds32(blk0 + 4 * q);
-        sw1[q] = lds32(blk1 + 4 * q);
+        sw0[q] = lds32(blk0 + 4 * q) & 0x0F0F0F0Fu;
+        sw1[q] = lds32(blk1 + 4 * q) & 0x0F0F0F0Fu;
     }
     const uint32_t dm0 = lds32(blk0 + 80), dm1 = lds32(blk1 + 80);
     // qs bytes 4cq..4cq+3 of each 16-byte quarter (2n + h)
@@ -283,8 +286,8 @@ __device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk
         const int sh = 2 * ((s >> 1) & 3);
         const uint32_t c0 = (qw0[nh] >> sh) & 0x03030303u;
         const uint32_t c1 = (qw1[nh] >> sh) & 0x03030303u;
-        const uint32_t k0 = __byte_perm(sw0[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3)) & 15u;
-        const uint32_t k1 = __byte_perm(sw1[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3)) & 15u;
+        const uint32_t k0 = __byte_perm(sw0[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3));
+        const uint32_t k1 = __byte_perm(sw1[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3));
         const uint32_t v0 = c0 * k0, v1 = c1 * k1;  // bytewise sc * q <= 45: no carries
         const uint32_t a0 = lo_pair(v0), a1 = lo_pair(v1), a2 = hi_pair(v0), a3 = hi_pair(v1);
         mma_bf16(acc, a0, a1, a2, a3, o.bx[s].x, o.bx[s].y);
@@ -322,14 +325,11 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(full_b + a.nst);
     int* done = reinterpret_cast<int*>(smem + a.off_cnt);  // warps finished with the slot's stage
     int* n_issued = done + a.nst;
-    int* next_issue = n_issued + 1;
-    int* summed = next_issue + 1;  // stages whose partial sums are in the rows
-    int* x_done = summed + 1;      // warps holding the current chunk's activations
+    int* x_done = n_issued + 1;    // warps holding the current chunk's activations
     int* x_issued = x_done + 1;    // activation chunks copied in
     uint64_t* xbar = full_b + a.nst + 1;
     uint8_t* xs = smem + a.off_x;
-    float4* red = reinterpret_cast<float4*>(smem + a.off_red);  // [nst][16 warps][32 lanes]
-    float* yacc = reinterpret_cast<float*>(smem + a.off_yacc);  // [rows of this CTA][8 tokens]
+    float* yacc = reinterpret_cast<float*>(smem + a.off_yacc);  // [16 warps][rows of this CTA][8 tokens]
 
     const int cta = blockIdx.x;
     const int tlo = cta * a.tiles_q + min(cta, a.tiles_r);
@@ -338,11 +338,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     const int nstages = ngroups * a.nchunks;
     const int crow0 = thi > tlo ? tile_at(a, tlo).crow : 0;
     const int pre = min(a.nst, nstages);
-    // CTAs start at different K chunks, so that they do not all read the
-    // same activations at the same moment.  Each chunk's sums go to their own
-    // accumulator and the chunks are added in K order at the end, so the
-    // result does not depend on the starting chunk.
-    const int c_first = a.ychunks > 1 ? cta % a.nchunks : 0;
 
     auto ring_pos = [&](int i, int& slot, uint32_t& parity) {
         const int q = (int)__umulhi((uint32_t)i, a.nst_magic);
@@ -356,8 +351,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             for (int s2 = 0; s2 < a.nst; ++s2)
                 done[s2] = 0;
             *n_issued = 0;
-            *next_issue = pre;
-            *summed = 0;
             *x_done = 0;
             *x_issued = 0;
             mbar_init(smem_u32(xbar), 1);
@@ -366,7 +359,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             mbar_init(smem_u32(&full_b[s2]), 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < a.yacc_rows * a.ychunks * kTok; i += blockDim.x)
+    for (int i = tid; i < kMtWarps * a.yacc_rows * kTok; i += blockDim.x)
         yacc[i] = 0.f;
     // global memory may still be written by the previous kernel in the stream
     pdl_wait();
@@ -380,7 +373,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         uint32_t parity;
         ring_pos(j, slot, parity);
         const int cs = j / ngroups;
-        const int c = cs + c_first < a.nchunks ? cs + c_first : cs + c_first - a.nchunks;
+        const int c = cs;
         const int t0 = tlo + (j - cs * ngroups) * a.tps;
         const int nbc_c = min(a.nbc, a.nb - c * a.nbc);
         const uint32_t piece = (uint32_t)nbc_c * kBlockBytes;  // bytes of a row in this chunk
@@ -424,98 +417,15 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         if (lane == 0)
             atomicAdd(n_issued, 1);
     };
-    // Add stage k's 16 partial sums, in warp order, into the CTA's rows
-    // (the whole warp; lane (g, cq) takes rows g, g+8 and tokens 2cq, 2cq+1).
-    auto sum_stage = [&](int k) {
-        int slot;
-        uint32_t parity;
-        ring_pos(k, slot, parity);
-        const int ck = k / ngroups;
-        const int t0 = tlo + (k - ck * ngroups) * a.tps;
-        const int ch = a.ychunks > 1 ? (ck + c_first) % a.nchunks : 0;
-        for (int tt = 0; tt < a.tps; ++tt) {
-            if (t0 + tt >= thi)
-                break;
-            const Tile t = tile_at(a, t0 + tt);
-            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = tt * a.nbc; w < (tt + 1) * a.nbc; ++w) {
-                const float4 p = red[((size_t)slot * kMtWarps + w) * 32 + lane];
-                sum.x += p.x;
-                sum.y += p.y;
-                sum.z += p.z;
-                sum.w += p.w;
-            }
-            const int ra = t.crow - crow0 + g;
-            float* y0 = yacc + ((size_t)ra * a.ychunks + ch) * kTok + 2 * cq;
-            float* y1 = yacc + ((size_t)(ra + 8) * a.ychunks + ch) * kTok + 2 * cq;
-            if (g < t.nrows) {
-                y0[0] += sum.x;
-                y0[1] += sum.y;
-            }
-            if (g + 8 < t.nrows) {
-                y1[0] += sum.z;
-                y1[1] += sum.w;
-            }
-        }
-    };
-    // Stage j is copied in by whichever warp claims it first, once every warp
-    // is done with its slot's previous stage (j - nst) and every earlier stage
-    // has been summed.  The claimer sums stage j - nst first, so partial sums
-    // reach the rows in stage order whichever warps do the work.
-    auto try_issue = [&]() {
-        int claim = -1;
-        if (lane == 0) {
-            const int j = *reinterpret_cast<volatile int*>(next_issue);
-            if (j < nstages) {
-                int sj;
-                uint32_t pj;
-                ring_pos(j, sj, pj);
-                if (*reinterpret_cast<volatile int*>(&done[sj]) == kMtWarps &&
-                    *reinterpret_cast<volatile int*>(summed) == j - a.nst && atomicCAS(next_issue, j, j + 1) == j) {
-                    __threadfence_block();
-                    claim = j;
-                }
-            }
-        }
-        claim = __shfl_sync(0xffffffffu, claim, 0);
-        if (claim >= 0) {
-            int sj;
-            uint32_t pj;
-            ring_pos(claim, sj, pj);
-            sum_stage(claim - a.nst);
-            __syncwarp();
-            if (lane == 0) {
-                atomicExch(&done[sj], 0);
-                __threadfence_block();
-                atomicExch(summed, claim - a.nst + 1);
-            }
-            produce(claim);
-        }
-    };
-    // Poll for a stage (claiming refills meanwhile); gives up after ~2 s.
+    // Wait for stage data; gives up after ~2 s.
     auto wait_stage = [&](int slot, uint32_t parity) -> bool {
-        const uint32_t bar = smem_u32(&full_b[slot]);
-        uint64_t t0 = 0;
-        for (uint32_t it = 0;; ++it) {
-            if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity)))
-                return true;
-            try_issue();
-            __nanosleep(64);
-            if ((it & 15u) == 15u) {
-                if (*abort_flag)
-                    return false;
-                const uint64_t now = global_timer_ns();
-                if (t0 == 0) {
-                    t0 = now;
-                } else if (now - t0 > 2000000000ull) {
-                    if (lane == 0) {
-                        atomicOr(&g_mt_error, Q2K_ERR_BIT_WAIT_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    return false;
-                }
-            }
+        const bool ok =
+            __all_sync(0xffffffffu, !*abort_flag && mbar_wait_bounded(smem_u32(&full_b[slot]), parity, abort_flag));
+        if (!ok && lane == 0) {
+            atomicOr(&g_mt_error, Q2K_ERR_BIT_WAIT_TIMEOUT);
+            *abort_flag = 1;
         }
+        return ok;
     };
 
     // Activations of K chunk c into shared memory (one thread): one bulk copy
@@ -540,16 +450,16 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     };
 
     if (tid == 0 && a.x_tma)
-        issue_x(c_first);  // the first activations ahead of the weights
+        issue_x(0);  // the first activations ahead of the weights
     if (warp < pre)
         produce(warp);
 
     const int tt_w = warp / a.nbc;          // this warp's tile within a stage
     const int bb_w = warp - tt_w * a.nbc;   // and its block within the K chunk
     bool aborted = false;
-    bool released_last = false;
+    float* yw = yacc + (size_t)warp * a.yacc_rows * kTok;  // this warp's accumulators
     BOps ops;  // this warp's B operands for the current K chunk
-    int c = c_first, gidx = 0, chunk_seq = 0;
+    int c = 0, gidx = 0, chunk_seq = 0;
     for (int i = 0; i < nstages; ++i) {
         if (gidx == 0) {
             const int kb = c * a.nbc + bb_w;
@@ -581,19 +491,28 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         ring_pos(i, slot, parity);
         const int t0 = tlo + gidx * a.tps;
         const int nbc_c = min(a.nbc, a.nb - c * a.nbc);
-        if (!aborted && !released_last)
-            try_issue();
         if (!aborted && !wait_stage(slot, parity))
             aborted = true;
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
         if (!aborted && bb_w < nbc_c && t0 + tt_w < thi) {
             const uint8_t* blk0 = ring + (size_t)slot * a.stage_bytes + (size_t)(tt_w * kTile + g) * a.rstride +
                                   (size_t)bb_w * kBlockBytes;
             const uint8_t* blk1 = blk0 + (size_t)8 * a.rstride;
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
             mt_block<ACT>(blk0, blk1, ops, cq, part);
+            // rows g and g+8 of the tile, tokens 2cq and 2cq+1: this warp's
+            // accumulators, added in chunk order
+            const Tile t = tile_at(a, t0 + tt_w);
+            float* y0 = yw + (size_t)(t.crow - crow0 + g) * kTok + 2 * cq;
+            if (g < t.nrows) {
+                y0[0] += part[0];
+                y0[1] += part[1];
+            }
+            if (g + 8 < t.nrows) {
+                y0[8 * kTok] += part[2];
+                y0[8 * kTok + 1] += part[3];
+            }
         }
-        red[((size_t)slot * kMtWarps + warp) * 32 + lane] = make_float4(part[0], part[1], part[2], part[3]);
-        // release (the stage is summed by the warp that claims its slot next)
+        // release; the last warp out refills the slot
         __syncwarp();
         int last = 0;
         if (lane == 0) {
@@ -601,7 +520,13 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             last = atomicAdd(&done[slot], 1) == kMtWarps - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        released_last = last != 0;
+        if (last) {
+            if (lane == 0)
+                done[slot] = 0;
+            __syncwarp();
+            if (i + a.nst < nstages && !*abort_flag)
+                produce(i + a.nst);
+        }
         if (++gidx == ngroups) {
             gidx = 0;
             if (++c == a.nchunks)
@@ -627,10 +552,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         __syncthreads();
         return;
     }
-    // the last stages (their slots were never claimed again) are summed here
-    if (warp == 0)
-        for (int k = *reinterpret_cast<volatile int*>(summed); k < nstages; ++k)
-            sum_stage(k);
     __syncthreads();
     // ---- outputs: rows of this CTA in order, token-major for coalescing ----
     if (thi > tlo) {
@@ -642,8 +563,8 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             const int seg = crow < a.N[0] ? 0 : 1;
             const int row = seg == 0 ? crow : crow - a.N[0];
             float v = 0.f;
-            for (int ch = 0; ch < a.ychunks; ++ch)
-                v += yacc[((size_t)r * a.ychunks + ch) * kTok + t];
+            for (int w = 0; w < kMtWarps; ++w)  // the warps' accumulators in warp order
+                v += yacc[((size_t)w * a.yacc_rows + r) * kTok + t];
             a.y[seg][(int64_t)t * a.ldy[seg] + row] = v;
         }
     }
@@ -746,8 +667,9 @@ cudaError_t launch_mt(const MvProblem& p, cudaStream_t s)
     a.tiles0 = (a.N[0] + kTile - 1) / kTile;
     a.tiles_total = a.tiles0 + (a.N[1] + kTile - 1) / kTile;
     // one CTA per SM; more CTAs (in waves) when a CTA would own more than
-    // 32 tiles, which bounds its per-row accumulators to 16.5 KB
-    const int grid = std::min(a.tiles_total, std::max(di.sm_count, (a.tiles_total + 31) / 32));
+    // kMtTilesPerCta tiles (each warp keeps an accumulator per row and token)
+    const int grid = std::min(a.tiles_total,
+                              std::max(di.sm_count, (a.tiles_total + kMtTilesPerCta - 1) / kMtTilesPerCta));
     a.tiles_q = a.tiles_total / grid;
     a.tiles_r = a.tiles_total % grid;
     a.rstride = (uint32_t)(a.nbc * kBlockBytes);
@@ -758,7 +680,6 @@ cudaError_t launch_mt(const MvProblem& p, cudaStream_t s)
     a.w_aligned = ((reinterpret_cast<uintptr_t>(a.W[0]) | reinterpret_cast<uintptr_t>(a.W[1])) & 15u) == 0 &&
                   a.nb % 4 == 0;
     a.yacc_rows = (a.tiles_q + 1) * kTile;
-    a.ychunks = a.nchunks <= 8 ? a.nchunks : 1;
     const size_t smem_cap = std::min<size_t>((size_t)di.smem_optin, 224 * 1024);
     size_t smem = 0;
     int nst = 8;
@@ -767,10 +688,8 @@ cudaError_t launch_mt(const MvProblem& p, cudaStream_t s)
         size_t off = (size_t)nst * a.stage_bytes;
         a.off_x = (uint32_t)off;
         off += a.x_tma ? (((size_t)a.m * a.xrs + 127) / 128 * 128) : 0;
-        a.off_red = (uint32_t)off;
-        off += (size_t)nst * kMtWarps * 32 * 16;
         a.off_yacc = (uint32_t)off;
-        off += mt_align16((size_t)a.yacc_rows * a.ychunks * kTok * sizeof(float));
+        off += mt_align16((size_t)kMtWarps * a.yacc_rows * kTok * sizeof(float));
         a.off_bar = (uint32_t)off;
         off += mt_align16((size_t)(nst + 2) * sizeof(uint64_t));
         a.off_cnt = (uint32_t)off;
