@@ -19,13 +19,13 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   on every host core (threads over output rows; the line's value).
 * --impl reference times the CPU oracle on the same workload on every host
   core (rank 0 only).
-* --ncu-case [mv|mt|gemm|small|q3k|mmq] runs a few untimed calls for a profiler
+* --ncu-case [mv|mt|gemm|small|q3k|mmq|moe] runs a few untimed calls for a profiler
   capture and prints no JSON line: mv = the headline kernel (bf16 GEMV) and
   the q8_1 MMVQ at m=1 on the headline shape; mt = the same shape at m=8
   (the tensor-core MMVQ); gemm = the dense bf16 GEMM at m=64 and m=256,
   N=K=16384; small = one call of every other kernel at the configurations'
   shapes; q3k = the Q3_K MMVQ at m=1 and 2; mmq = the Q2_K matmul for many
-  tokens at m=64 and m=256, N=K=16384.
+  tokens at m=64 and m=256, N=K=16384; moe = the MoE step on 8 experts.
 * --all also times every configuration of the sweep and prints one JSON
   object per configuration to stderr (and to the file --all-out names).
 With torchrun (N > 1) every rank runs an independent replica (the path is
@@ -767,7 +767,8 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     m=256, N=K=16384 (537 MB of bf16 weights), one call each.  q3k:
     `calls` calls of q3k_mmvq_q8_1 at m=1, then at m=2, N=K=16384 (115 MB of
     Q3_K weights).  mmq: q2k_mmq_bf16 at m=64, then m=256, N=K=16384 (88 MB
-    of Q2_K weights), one call each."""
+    of Q2_K weights), one call each.  moe: `calls` calls of q2k_moe_m1 on
+    the configuration's 8 selected experts (66 MB)."""
     import torch
     from mmvq_q2_gb300 import build as b
     b.build()
@@ -785,6 +786,19 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
             xq = q.q8_1_quantize_rows(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
             for _ in range(calls):
                 q.q3k_mmvq_q8_1(Wd, xq, K_HEAD)
+        torch.cuda.synchronize()
+        print("ncu case done", file=sys.stderr)
+        return
+    if which == "moe":
+        dim, inter, E = 4096, 2048, 8
+        mats = [torch.from_numpy(synth.q2k_matrix(0, f"ncu.moe.{kind}{e}", *shape)).cuda()
+                for kind, shape in (("gate", (inter, dim)), ("up", (inter, dim)), ("down", (dim, inter)))
+                for e in range(E)]
+        x = torch.from_numpy(synth.bf16_normal(0, "cfg3.x", (dim,)).view(np.int16)).cuda().view(torch.bfloat16)
+        w = torch.full((E,), 1.0 / E, dtype=torch.float32, device="cuda")
+        tbl = q.pointer_table(mats)
+        for _ in range(calls):
+            q.q2k_moe_m1(tbl, E, dim, inter, x, w)
         torch.cuda.synchronize()
         print("ncu case done", file=sys.stderr)
         return
@@ -827,7 +841,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
     ap.add_argument("--all-out", default=None, help="also write the --all records here, one JSON object a line")
-    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k", "mmq"], default=None)
+    ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k", "mmq", "moe"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
