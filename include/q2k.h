@@ -169,7 +169,7 @@ int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx
  * The activations enter the integer dot products as 16-bit fixed point
  * with one power-of-two exponent per 16 values (exact unless a group spans
  * more than 2^7 in magnitude; then the smallest lose bits below 2^-15 of
- * the group maximum).  One token over rows of K >= 8192 uses one exponent
+ * the group maximum).  One token over rows of K >= 4096 uses one exponent
  * per 32 values and a 2^14 range (exact within 2^6 of the group maximum,
  * bits below 2^-14 of it lost).  Groups below 2^-100 count as zero. */
 int q2k_gemv_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx,
@@ -194,10 +194,11 @@ int q2k_mmvq_pair(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t
  *   x_bf16  [m, K] bf16 rows back to back
  *   xq_out  m q8_1 rows; receives q8_1_quantize_rows(x) in every case
  *   Wa, Na, ya, Wb, Nb, yb, K, m  as for q2k_mmvq_pair
- * For m = 1 and a 16-byte aligned x the encoding runs inside the pair
- * launch (each CTA encodes the row; one launch).  Otherwise it is a launch
- * of its own, then the pair.  Either way xq_out, ya and yb equal the two
- * separate calls bit for bit. */
+ * For m = 1, a 16-byte aligned x and rows outside 16..128 blocks (K %
+ * 1024 == 0) the encoding runs inside the pair launch (each CTA encodes the
+ * row; one launch).  Otherwise it is a launch of its own, then the pair
+ * (rows of 16..128 blocks run a kernel for which that is faster).  Either
+ * way xq_out, ya and yb equal the two separate calls bit for bit. */
 int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, int64_t Nb, float* yb,
                        int64_t K, const uint16_t* x_bf16, int64_t m, void* xq_out, q2k_stream_t stream);
 

@@ -339,8 +339,11 @@ int q2k_mmvq_pair_bf16(const void* Wa, int64_t Na, float* ya, const void* Wb, in
     p.ldy[0] = Na;
     p.ldy[1] = Nb;
     p.x_tok_stride = (int64_t)q8_1_row_bytes(K);
-    if (m == 1 && aligned(x_bf16, 16)) {
-        // one launch: every CTA encodes the row, the first also stores it
+    p.x = xq_out;
+    if (m == 1 && aligned(x_bf16, 16) && !m1_supported(p)) {
+        // one launch: every CTA encodes the row, the first also stores it.
+        // (Where the row-team kernel takes the pair, a separate encoding
+        // launch ahead of it measured faster: 4.5 vs 6.0 us at cfg2.)
         p.x = x_bf16;
         p.x_prep = 1;
         p.x_out = xq_out;

@@ -317,12 +317,12 @@ bool plan_m1(const MvProblem& p, const DeviceInfo& di, M1Args& a, int& grid, siz
     const bool tokens_ok = p.m == 1 || p.m == 2 || (p.m == 4 && p.act == ACT_Q8);
     if (!tokens_ok || p.W_table || p.w_seg_stride || p.x_prep || p.n_seg < 1 || p.n_seg > 2)
         return false;
-    // One token: rows of 32..128 blocks, the rows the general kernel also
-    // walks with 128-weight slices, so the two give the same bits (the pair
-    // from bf16 and the expert batches run there and promise equality with
-    // this one).  Several tokens: rows of 8..128 blocks (no other path
-    // promises their bits).
-    const int64_t kmin = (p.m == 1 ? 32 : 8) * (int64_t)kBlockWeights;
+    // One token: rows of 16..128 blocks, the rows the general kernel also
+    // walks with 128-weight slices and the same reduction, so the two give
+    // the same bits (the pair from bf16 and the expert batches run there and
+    // promise equality with this one).  Several tokens: rows of 8..128
+    // blocks (no other path promises their bits).
+    const int64_t kmin = (p.m == 1 ? 16 : 8) * (int64_t)kBlockWeights;
     if (p.K % 1024 || p.K < kmin || p.K > 128 * kBlockWeights)
         return false;
     const int nseg = p.n_seg;

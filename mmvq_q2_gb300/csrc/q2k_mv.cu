@@ -630,13 +630,14 @@ cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
     return launch_pdl(k, dim3((unsigned)grid), dim3((unsigned)a.tc), smem, s, a);
 }
 
-// Qs words per thread slice.  One token over a long row takes 8-word
-// slices (128 weights: the per-row scale, min and load work is spread over
-// twice the weights); short rows keep 4-word slices, so enough threads
-// share each row.
+// Qs words per thread slice.  One token over a row of 16 blocks or more
+// takes 8-word slices (128 weights: the per-row scale, min and load work is
+// spread over twice the weights; the single-call kernel of q2k_m1.cu walks
+// such rows the same way, and the two must give the same bits); shorter rows
+// keep 4-word slices, so enough threads share each row.
 int sw_for(int act, int m, int64_t nb)
 {
-    if (m == 1 && nb >= 32)
+    if (m == 1 && nb >= 16)
         return 8;
     if (act == ACT_Q8)
         return m <= 4 ? 4 : 2;
