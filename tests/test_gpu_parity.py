@@ -237,6 +237,26 @@ def test_mmvq_q8_1_long_rows_one_token(lib, N, K):
         assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_Q8
 
 
+# the row-team kernel's widths: one token at 16..31 blocks per row, two or
+# four tokens at 8..31 (teams of a power of two of lanes: 20 and 28 blocks
+# leave lanes idle), ragged row counts
+TEAM_WIDTHS = [(1, 4096, 37), (1, 5120, 1000), (1, 7168, 300), (2, 2048, 300), (2, 3072, 1000), (2, 5120, 37),
+               (4, 2048, 1000), (4, 3072, 300)]
+
+
+@pytest.mark.parametrize("m,K,N", TEAM_WIDTHS)
+def test_row_team_widths_against_oracle(lib, m, K, N):
+    W = synth.q2k_matrix(30, f"team.{N}.{K}", N, K)
+    x = synth.bf16_normal(30, f"team.x.{m}.{K}", (m, K))
+    Wd = dev(W)
+    if m <= 2:
+        y = lib.q2k_gemv_bf16(Wd, bf16_dev(x)).cpu().numpy()
+        assert rel_err_rows(y, oracle.matvec(W, N, K, x_f64(x))) <= TOL_BF16
+    xq = oracle.q8_1_quantize(x)
+    y8 = lib.q2k_mmvq_q8_1(Wd, dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y8, oracle.matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= 1e-4
+
+
 def _q8_rows_at_a_rounding_edge(m, K):
     """q8_1 rows whose every 32-value block has d = 1285 * 2^-16 (exact in
     fp16) and one q = 51: a slice's group sum d*51 has the mantissa
