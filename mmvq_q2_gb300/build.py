@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libq2k.so")
-SOURCES = ["q2k_api.cu", "q2k_mv.cu", "q2k_m1.cu", "q2k_mmq.cu", "q2k_mt.cu", "q2k_small.cu", "q2k_gemm.cu", "q2k_umma.cu", "q3k_mv.cu"]
+SOURCES = ["q2k_api.cu", "q2k_mv.cu", "q2k_m1.cu", "q2k_mmq.cu", "q2k_mt.cu", "q2k_small.cu", "q2k_gemm.cu", "q2k_umma.cu", "q3k_mv.cu", "q3k_mt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -126,7 +126,7 @@ int q2k_device_error(int32_t* host_out, int clear)
 {
     if (!host_out)
         return Q2K_ERR_NULL_ARG;
-    int32_t a = 0, b = 0, c = 0, d = 0, q = 0, o = 0, mq = 0;
+    int32_t a = 0, b = 0, c = 0, d = 0, q = 0, o = 0, mq = 0, q3t = 0;
     cudaError_t e = mv_error_word(&a, clear != 0);
     if (e == cudaSuccess)
         e = m1_error_word(&o, clear != 0);
@@ -140,9 +140,11 @@ int q2k_device_error(int32_t* host_out, int clear)
         e = umma_error_word(&d, clear != 0);
     if (e == cudaSuccess)
         e = q3_error_word(&q, clear != 0);
+    if (e == cudaSuccess)
+        e = q3mt_error_word(&q3t, clear != 0);
     if (e != cudaSuccess)
         return fail_cuda(e);
-    *host_out = a | b | c | d | q | o | mq;
+    *host_out = a | b | c | d | q | o | mq | q3t;
     return Q2K_OK;
 }
 

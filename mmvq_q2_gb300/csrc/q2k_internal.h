@@ -116,6 +116,11 @@ struct Q3Problem {
     int64_t y_seg_stride;  // floats between segments
 };
 cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s);
+// The same for m >= kQ3MtMinTokens tokens on one matrix, on the tensor
+// cores (q3k_mt.cu); launch_q3k_mv routes those problems here.
+constexpr int kQ3MtMinTokens = 3;
+bool q3mt_supported(const Q3Problem& p);
+cudaError_t launch_q3k_mt(const Q3Problem& p, cudaStream_t s);
 
 // Read (and optionally clear) this translation unit's device error word.
 cudaError_t mv_error_word(int32_t* out, bool clear);
@@ -125,5 +130,6 @@ cudaError_t gemm_error_word(int32_t* out, bool clear);
 cudaError_t mt_error_word(int32_t* out, bool clear);
 cudaError_t umma_error_word(int32_t* out, bool clear);
 cudaError_t q3_error_word(int32_t* out, bool clear);
+cudaError_t q3mt_error_word(int32_t* out, bool clear);
 
 }  // namespace q2k

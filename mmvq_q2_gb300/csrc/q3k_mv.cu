@@ -402,6 +402,8 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
+    if (q3mt_supported(p))  // several tokens: the tensor-core kernel
+        return launch_q3k_mt(p, s);
     const int nb = (int)(p.K / 256);
     // tokens per walk over the rows: one, or pairs (groups of four tokens
     // in 4-byte slices measured slower: 188 vs 103 us for m = 4 at 16384^2)

@@ -79,7 +79,7 @@ def test_q3k_mmvq_long_rows_many_chunks(lib, m):
     assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= TOL_EXACT_X
 
 
-@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("m", [1, 2, 3])
 def test_q3k_mmvq_largest_k(lib, m):
     # K = 2^20, the largest the boundary accepts: 4096 block columns, 256
     # (one token) or 512 chunks per row, one row per CTA
@@ -91,18 +91,33 @@ def test_q3k_mmvq_largest_k(lib, m):
     assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= TOL_EXACT_X
 
 
-@pytest.mark.parametrize("K", [512, 4096, 4864])
-def test_q3k_mmvq_weights_off_a_16_byte_boundary(lib, K):
-    # the matrix starts 4 bytes into its buffer: every block's word phase flips
-    N, m = 50, 2
+@pytest.mark.parametrize("K,m", [(512, 2), (4096, 2), (4864, 2), (4096, 4), (4864, 6), (2048, 8)])
+def test_q3k_mmvq_weights_off_a_16_byte_boundary(lib, K, m):
+    # the matrix starts 4 bytes into its buffer: every block's word phase
+    # flips, and several tokens take warp copies instead of tensor copies
+    N = 50
     W = synth.q3k_matrix(5, f"q3.off.{K}", N, K)
     buf = torch.zeros(W.size + 4, dtype=torch.uint8, device="cuda")
     buf[4:] = dev(W.reshape(-1))
-    x = synth.bf16_normal(5, f"q3.off.x.{K}", (m, K))
+    x = synth.bf16_normal(5, f"q3.off.x.{K}.{m}", (m, K))
     xq = dev(oracle.q8_1_quantize(x))
     y = lib.q3k_mmvq_q8_1(buf[4:], xq, K).cpu().numpy()
     assert np.array_equal(y, lib.q3k_mmvq_q8_1(dev(W), xq, K).cpu().numpy())
     assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq.cpu().numpy(), m, K))) <= TOL_EXACT_X
+
+
+@pytest.mark.parametrize("N,K,m", [(50, 4096, 5), (40, 1280, 3)])
+def test_q3k_mmvq_activations_off_a_16_byte_boundary(lib, N, K, m):
+    # q8_1 rows 4 bytes into their buffer: several tokens read them from
+    # global memory instead of staging them by bulk copy, with the same bits
+    W = dev(synth.q3k_matrix(12, f"q3.xoff.{K}", N, K))
+    xq = oracle.q8_1_quantize(synth.bf16_normal(12, f"q3.xoff.x.{K}", (m, K)))
+    buf = torch.zeros(xq.size + 4, dtype=torch.uint8, device="cuda")
+    buf[4:] = dev(xq.reshape(-1))
+    y = lib.q3k_mmvq_q8_1(W, buf[4:].view(m, -1), K)
+    assert torch.equal(y, lib.q3k_mmvq_q8_1(W, dev(xq), K))
+    ref = oracle.q3k_matvec(W.cpu().numpy(), N, K, oracle.q8_1_dequant(xq, m, K))
+    assert rel_err_rows(y.cpu().numpy(), ref) <= TOL_EXACT_X
 
 
 def test_q3k_mmvq_output_stride_leaves_the_gap(lib):
