@@ -765,8 +765,8 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     q2k_gemv_bf16, then of q2k_mmvq_q8_1, at m=1 N=K=16384 (88 MB of
     weights).  mt: the same at m=8.  gemm: dense_gemm_bf16 at m=64, then
     m=256, N=K=16384 (537 MB of bf16 weights), one call each.  q3k:
-    `calls` calls of q3k_mmvq_q8_1 at m=1, then at m=2, N=K=16384 (115 MB of
-    Q3_K weights).  mmq: q2k_mmq_bf16 at m=64, then m=256, N=K=16384 (88 MB
+    `calls` calls of q3k_mmvq_q8_1 at m=1, then at m=2, then at m=8,
+    N=K=16384 (115 MB of Q3_K weights).  mmq: q2k_mmq_bf16 at m=64, then m=256, N=K=16384 (88 MB
     of Q2_K weights), one call each.  moe: `calls` calls of q2k_moe_m1 on
     the configuration's 8 selected experts (66 MB)."""
     import torch
@@ -781,7 +781,7 @@ def run_ncu_case(which: str = "mv", calls: int = 3):
     if which == "q3k":
         W = synth.q3k_matrix(0, "sweep.q3.W16384", N_HEAD, K_HEAD)
         Wd = torch.from_numpy(W).cuda()
-        for m in (1, 2):
+        for m in (1, 2, 8):
             x = synth.bf16_normal(0, f"sweep.q3.x{m}", (m, K_HEAD))
             xq = q.q8_1_quantize_rows(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
             for _ in range(calls):

@@ -9,11 +9,13 @@
 // (mma.sync m16n8k16, bf16 in, fp32 accumulate):
 //
 //   A[r][e] = 128 + sc_s(r) * q(r, 16 s + e)      exact small integers in bf16
-//   B[e][t] = x_t[256 b + 16 s + e]                bf16 activations (exact), or
-//                                                  the q8_1 values d8*q split
-//                                                  into a bf16 high and low part
+//   B[e][t] = x_t[256 b + 16 s + e]                bf16 activations (exact)
 //
-// for sub-block s of block b, row r and token t.  Inside a sub-block the
+// for sub-block s of block b, row r and token t.  With q8_1 activations both
+// operands are fp16 integers instead: A = 1024 + sc*q, B = the q8 values,
+// and the accumulator input of a plane's first MMA is -1024 times the sum of
+// its 32 q8 values, so the two MMAs of plane c (sub-blocks 2c, 2c+1, one
+// q8_1 block) give sum sc*q*q8 exactly; it is scaled by d8 per plane.  Inside a sub-block the
 // MMA's k order is permuted the same way on both sides: the thread that
 // holds MMA k = 2c, 2c+1, 2c+8, 2c+9 takes weights and activations 4c..4c+3,
 // so it reads one aligned qs word and 8 contiguous bytes of activations.  The constant 128 is added
@@ -79,7 +81,7 @@ struct MtArgs {
     uint32_t rstride;      // bytes per row in a stage (nbc * 84)
     int w_aligned;         // every copied row piece is 16-byte aligned
     int yacc_rows;         // rows per warp accumulator: at most kMtTilesPerCta tiles
-    uint32_t off_x, off_yacc, off_bar, off_cnt;
+    uint32_t off_x, off_pl, off_yacc, off_bar, off_cnt;
 };
 
 struct Tile {
@@ -104,6 +106,16 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
 // 2-D tensor copy of box {x, y} (8-byte elements) into shared memory.
@@ -148,20 +160,39 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (ui
 // (each byte < 128): the byte becomes the mantissa under the exponent of 128.
 __device__ __forceinline__ uint32_t lo_pair(uint32_t v) { return __byte_perm(v, 0x43434343u, 0x4140u); }
 __device__ __forceinline__ uint32_t hi_pair(uint32_t v) { return __byte_perm(v, 0x43434343u, 0x4342u); }
+// The same under the fp16 exponent of 1024 (each byte < 256).
+__device__ __forceinline__ uint32_t lo_pair16(uint32_t v) { return __byte_perm(v, 0x64646464u, 0x4140u); }
+__device__ __forceinline__ uint32_t hi_pair16(uint32_t v) { return __byte_perm(v, 0x64646464u, 0x4342u); }
+
+// Two q8 values (signed bytes of w picked by SEL) as an exact fp16 pair: the
+// bytes, offset by 128, go under the exponent of 1024 and 1152 comes off.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t q8_pair_f16(uint32_t w)
+{
+    const uint32_t biased = __byte_perm(w ^ 0x80808080u, 0x64646464u, SEL);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&biased),
+                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 
 // This warp's operands for block bb (all tokens), read from global memory
 // (the activations are small and L2-resident):
-//  bx/bxl  main MMA B fragments of the 16 sub-blocks: lane 4g + cq gets x_g
-//          at 16 s + 2cq, +1, +8, +9 (bf16 activations exactly; q8_1 values
-//          d8*q as a bf16 high part and low part)
-//  bmh/bml min MMA B fragment: sub-block sums of x_g for sub-blocks 2cq,
-//          2cq+1, 2cq+8, 2cq+9, as bf16 high and low parts
-//  xa, xm  for tokens 2cq and 2cq+1: what the main and the min MMA multiply
-//          by the constant 128 (the sums of their B operands over the block)
+//  bx      main MMA B fragments of the 16 sub-blocks: lane 4g + cq gets x_g
+//          at 16 s + 4cq .. 4cq+3 (bf16 activations exactly; with q8_1 the
+//          q8 values as fp16)
+//  bmh/bml min MMA B fragment: sub-block sums of x_g for sub-blocks 4cq..4cq+3,
+//          as bf16 high and low parts
+//  xa, xm  for tokens 2cq and 2cq+1: what the main (bf16 only) and the min
+//          MMA multiply by the constant 128 (the sums of their B operands
+//          over the block)
+//  pl      q8_1 only, the warp's table in shared memory: pl[4c + cq] for
+//          plane c (sub-blocks 2c, 2c+1) holds, for tokens 2cq and 2cq+1,
+//          the first MMA's accumulator input -1024 * (sum of the 32 q8
+//          values) and d8
 // Tokens m..7 (and blocks past the row) are zero.
 struct BOps {
-    uint2 bx[16], bxl[16];
+    uint2 bx[16];
     uint2 bmh, bml;
     float xa0, xa1, xm0, xm1;
 };
@@ -171,22 +202,24 @@ struct BOps {
 // the block's index from xrow0; live_b: the block exists.
 template <int ACT, bool SMEM>
 __device__ __forceinline__ void load_b(const MtArgs& a, const uint8_t* xrow0, int64_t xstride, int kb, bool live_b,
-                                       int lane, BOps& o)
+                                       int lane, BOps& o, float4* pl)
 {
     const int g = lane >> 2, cq = lane & 3;
     const bool live = g < a.m && live_b;
     const uint8_t* xt = xrow0 + (int64_t)(live ? g : 0) * xstride;
     const uint64_t keep = l2_policy_evict_last();
     const int bb = live ? kb : 0;
-    float ps[16], pa[16];  // this lane's share of each sub-block sum (exact x, and B's values)
+    float ps[16];      // this lane's share of each sub-block sum of x
+    int isum[16];      // q8_1: the same of the q8 values
+    float d8c[8];      // q8_1: d8 of each plane
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
         const int k0 = bb * kBlockWeights + 16 * s + 4 * cq;  // activations k0..k0+3
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (live) {
-            if constexpr (ACT == ACT_BF16) {
+        if constexpr (ACT == ACT_BF16) {
+            uint32_t w0 = 0u, w1 = 0u;
+            if (live) {
                 const uint8_t* p = xt + 2 * (int64_t)k0;
-                uint32_t w0, w1;
                 if (SMEM) {
                     const uint2 u = *reinterpret_cast<const uint2*>(p);
                     w0 = u.x;
@@ -200,31 +233,26 @@ __device__ __forceinline__ void load_b(const MtArgs& a, const uint8_t* xrow0, in
                     w0 = pack2(__ldg(p16), __ldg(p16 + 1));
                     w1 = pack2(__ldg(p16 + 2), __ldg(p16 + 3));
                 }
-                v[0] = __uint_as_float(w0 << 16);
-                v[1] = __uint_as_float(w0 & 0xFFFF0000u);
-                v[2] = __uint_as_float(w1 << 16);
-                v[3] = __uint_as_float(w1 & 0xFFFF0000u);
-            } else {
-                const uint8_t* qb = xt + (int64_t)(k0 >> 5) * kQ8Bytes;
-                const float d8 = half_lo_f(SMEM ? lds32(qb) : ldg32_keep(qb, keep));
-                const uint32_t qv = SMEM ? lds32(qb + 4 + (k0 & 31)) : ldg32_keep(qb + 4 + (k0 & 31), keep);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v[i] = d8 * (float)(int8_t)(qv >> (8 * i));  // exact in fp32
             }
+            v[0] = __uint_as_float(w0 << 16);
+            v[1] = __uint_as_float(w0 & 0xFFFF0000u);
+            v[2] = __uint_as_float(w1 << 16);
+            v[3] = __uint_as_float(w1 & 0xFFFF0000u);
+            o.bx[s] = make_uint2(w0, w1);
+        } else {
+            float d8 = 0.f;
+            uint32_t qv = 0u;
+            if (live) {
+                const uint8_t* qb = xt + (int64_t)(k0 >> 5) * kQ8Bytes;
+                d8 = half_lo_f(SMEM ? lds32(qb) : ldg32_keep(qb, keep));
+                qv = SMEM ? lds32(qb + 4 + (k0 & 31)) : ldg32_keep(qb + 4 + (k0 & 31), keep);
+            }
+            o.bx[s] = make_uint2(q8_pair_f16<0x4140u>(qv), q8_pair_f16<0x4342u>(qv));
+            isum[s] = dp4a_us(0x01010101u, qv, 0);
+            d8c[s >> 1] = d8;
         }
-        uint16_t h[4], l[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            h[i] = bf16_bits(v[i]);
-            l[i] = ACT == ACT_BF16 ? (uint16_t)0 : bf16_bits(v[i] - bf16_val(h[i]));
-        }
-        o.bx[s] = make_uint2(pack2(h[0], h[1]), pack2(h[2], h[3]));
-        o.bxl[s] = make_uint2(pack2(l[0], l[1]), pack2(l[2], l[3]));
-        ps[s] = (v[0] + v[1]) + (v[2] + v[3]);
-        pa[s] = ACT == ACT_BF16 ? ps[s]
-                                : ((bf16_val(h[0]) + bf16_val(l[0])) + (bf16_val(h[1]) + bf16_val(l[1]))) +
-                                      ((bf16_val(h[2]) + bf16_val(l[2])) + (bf16_val(h[3]) + bf16_val(l[3])));
+        // q8_1: d8 times the exact integer sum (one rounding)
+        ps[s] = ACT == ACT_BF16 ? (v[0] + v[1]) + (v[2] + v[3]) : d8c[s >> 1] * (float)isum[s];
     }
     // sub-block sums over the four lanes of token g (same order in every lane)
     float xa = 0.f, xm = 0.f;
@@ -233,10 +261,8 @@ __device__ __forceinline__ void load_b(const MtArgs& a, const uint8_t* xrow0, in
     for (int s = 0; s < 16; ++s) {
         float t = ps[s] + __shfl_xor_sync(0xffffffffu, ps[s], 1);
         t += __shfl_xor_sync(0xffffffffu, t, 2);
-        float u = pa[s] + __shfl_xor_sync(0xffffffffu, pa[s], 1);
-        u += __shfl_xor_sync(0xffffffffu, u, 2);
         const uint16_t hs = bf16_bits(t);
-        xa += u;
+        xa += t;
         xm += bf16_val(hs) + bf16_val(bf16_bits(t - bf16_val(hs)));
         if ((s >> 2) == cq)  // this lane's min-MMA positions: sub-blocks 4cq..4cq+3
             mine[s & 3] = t;
@@ -254,15 +280,30 @@ __device__ __forceinline__ void load_b(const MtArgs& a, const uint8_t* xrow0, in
     o.xa1 = __shfl_sync(0xffffffffu, xa, 8 * cq + 4);
     o.xm0 = __shfl_sync(0xffffffffu, xm, 8 * cq);
     o.xm1 = __shfl_sync(0xffffffffu, xm, 8 * cq + 4);
+    if constexpr (ACT != ACT_BF16) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            int S = isum[2 * c] + isum[2 * c + 1];
+            S += __shfl_xor_sync(0xffffffffu, S, 1);
+            S += __shfl_xor_sync(0xffffffffu, S, 2);
+            const float cs = -1024.f * (float)S;  // exact: |S| <= 4064
+            const float4 v = make_float4(__shfl_sync(0xffffffffu, cs, 8 * cq), __shfl_sync(0xffffffffu, cs, 8 * cq + 4),
+                                         __shfl_sync(0xffffffffu, d8c[c], 8 * cq),
+                                         __shfl_sync(0xffffffffu, d8c[c], 8 * cq + 4));
+            if (g == 0)
+                pl[4 * c + cq] = v;
+        }
+        __syncwarp();
+    }
 }
 
 // One 16-row tile by one Q2_K block (256 weights of each row) against the
-// tokens: 16 main MMAs (two with q8_1 activations), 2 min MMAs, then the
-// d / dmin scaling into this thread's four outputs (rows g, g+8; tokens
-// 2cq, 2cq+1).
+// tokens: 16 main MMAs, 2 min MMAs, then the d / dmin (and, with q8_1, the
+// per-plane d8) scaling into this thread's four outputs (rows g, g+8;
+// tokens 2cq, 2cq+1).
 template <int ACT>
-__device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk1, const BOps& o, int cq,
-                                         float (&part)[4])
+__device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk1, const BOps& o,
+                                         const float4* pl_tab, int cq, float (&part)[4])
 {
     uint32_t sw0[4], sw1[4];  // scale nibbles of sub-blocks 0..15, one per byte
 #pragma unroll
@@ -278,21 +319,44 @@ __device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk
         qw0[nh] = lds32(blk0 + 16 + 16 * nh + 4 * cq);
         qw1[nh] = lds32(blk1 + 16 + 16 * nh + 4 * cq);
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        // sub-block s = 8n + 2j + h: codes at bits 2j of quarter 2n + h
+    // bytes sc*q <= 45 of sub-block s = 8n + 2j + h: codes at bits 2j of
+    // quarter 2n + h, times the scale (bytewise, no carries)
+    auto scaled = [&](int s, uint32_t& v0, uint32_t& v1) {
         const int nh = ((s >> 3) << 1) | (s & 1);
         const int sh = 2 * ((s >> 1) & 3);
         const uint32_t c0 = (qw0[nh] >> sh) & 0x03030303u;
         const uint32_t c1 = (qw1[nh] >> sh) & 0x03030303u;
         const uint32_t k0 = __byte_perm(sw0[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3));
         const uint32_t k1 = __byte_perm(sw1[s >> 2], 0u, 0x4440u | (uint32_t)(s & 3));
-        const uint32_t v0 = c0 * k0, v1 = c1 * k1;  // bytewise sc * q <= 45: no carries
-        const uint32_t a0 = lo_pair(v0), a1 = lo_pair(v1), a2 = hi_pair(v0), a3 = hi_pair(v1);
-        mma_bf16(acc, a0, a1, a2, a3, o.bx[s].x, o.bx[s].y);
-        if constexpr (ACT != ACT_BF16)
-            mma_bf16(acc, a0, a1, a2, a3, o.bxl[s].x, o.bxl[s].y);
+        v0 = c0 * k0;
+        v1 = c1 * k1;
+    };
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (ACT == ACT_BF16) {
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            uint32_t v0, v1;
+            scaled(s, v0, v1);
+            mma_bf16(acc, lo_pair(v0), lo_pair(v1), hi_pair(v0), hi_pair(v1), o.bx[s].x, o.bx[s].y);
+        }
+    } else {
+        // plane c: sub-blocks 2c and 2c+1 share one q8_1 block
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 pl = pl_tab[4 * c + cq];
+            float d[4];
+            uint32_t v0, v1;
+            scaled(2 * c, v0, v1);
+            mma_f16(d, lo_pair16(v0), lo_pair16(v1), hi_pair16(v0), hi_pair16(v1), o.bx[2 * c].x, o.bx[2 * c].y,
+                    pl.x, pl.y, pl.x, pl.y);
+            scaled(2 * c + 1, v0, v1);
+            mma_f16(d, lo_pair16(v0), lo_pair16(v1), hi_pair16(v0), hi_pair16(v1), o.bx[2 * c + 1].x,
+                    o.bx[2 * c + 1].y, d[0], d[1], d[2], d[3]);
+            acc[0] = fmaf(pl.z, d[0], acc[0]);
+            acc[1] = fmaf(pl.w, d[1], acc[1]);
+            acc[2] = fmaf(pl.z, d[2], acc[2]);
+            acc[3] = fmaf(pl.w, d[3], acc[3]);
+        }
     }
     // min term: A = 128 + m over sub-blocks 4cq..4cq+3 (scale bytes 4cq..4cq+3)
     const uint32_t m0 = (lds32(blk0 + 4 * cq) >> 4) & 0x0F0F0F0Fu;
@@ -302,7 +366,7 @@ __device__ __forceinline__ void mt_block(const uint8_t* blk0, const uint8_t* blk
     mma_bf16(accm, lo_pair(m0), lo_pair(m1), hi_pair(m0), hi_pair(m1), o.bml.x, o.bml.y);
     const float d0 = half_lo_f(dm0), n0 = half_hi_f(dm0);
     const float d1 = half_lo_f(dm1), n1 = half_hi_f(dm1);
-    const float xa0 = 128.f * o.xa0, xa1 = 128.f * o.xa1;
+    const float xa0 = ACT == ACT_BF16 ? 128.f * o.xa0 : 0.f, xa1 = ACT == ACT_BF16 ? 128.f * o.xa1 : 0.f;
     const float xm0 = 128.f * o.xm0, xm1 = 128.f * o.xm1;
     part[0] += d0 * (acc[0] - xa0) - n0 * (accm[0] - xm0);
     part[1] += d0 * (acc[1] - xa1) - n0 * (accm[1] - xm1);
@@ -329,6 +393,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     int* x_issued = x_done + 1;    // activation chunks copied in
     uint64_t* xbar = full_b + a.nst + 1;
     uint8_t* xs = smem + a.off_x;
+    float4* plw = reinterpret_cast<float4*>(smem + a.off_pl) + warp * 32;  // this warp's per-plane q8_1 scalars
     float* yacc = reinterpret_cast<float*>(smem + a.off_yacc);  // [16 warps][rows of this CTA][8 tokens]
 
     const int cta = blockIdx.x;
@@ -468,7 +533,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 // warp to take its operands copies the next chunk in
                 if (!aborted && !wait_x((uint32_t)chunk_seq & 1u))
                     aborted = true;
-                load_b<ACT, true>(a, xs, a.xrs, bb_w, kb < a.nb, lane, ops);
+                load_b<ACT, true>(a, xs, a.xrs, bb_w, kb < a.nb, lane, ops, plw);
                 __syncwarp();
                 int lastx = 0;
                 if (lane == 0) {
@@ -482,7 +547,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                     }
                 }
             } else {
-                load_b<ACT, false>(a, a.x, a.x_tok_stride, kb, kb < a.nb, lane, ops);
+                load_b<ACT, false>(a, a.x, a.x_tok_stride, kb, kb < a.nb, lane, ops, plw);
             }
             ++chunk_seq;
         }
@@ -498,7 +563,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                                   (size_t)bb_w * kBlockBytes;
             const uint8_t* blk1 = blk0 + (size_t)8 * a.rstride;
             float part[4] = {0.f, 0.f, 0.f, 0.f};
-            mt_block<ACT>(blk0, blk1, ops, cq, part);
+            mt_block<ACT>(blk0, blk1, ops, plw, cq, part);
             // rows g and g+8 of the tile, tokens 2cq and 2cq+1: this warp's
             // accumulators, added in chunk order
             const Tile t = tile_at(a, t0 + tt_w);
@@ -688,6 +753,8 @@ cudaError_t launch_mt(const MvProblem& p, cudaStream_t s)
         size_t off = (size_t)nst * a.stage_bytes;
         a.off_x = (uint32_t)off;
         off += a.x_tma ? (((size_t)a.m * a.xrs + 127) / 128 * 128) : 0;
+        a.off_pl = (uint32_t)off;
+        off += q8 ? (size_t)kMtWarps * 32 * sizeof(float4) : 0;
         a.off_yacc = (uint32_t)off;
         off += mt_align16((size_t)kMtWarps * a.yacc_rows * kTok * sizeof(float));
         a.off_bar = (uint32_t)off;
