@@ -633,11 +633,16 @@ cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
 // Qs words per thread slice.  One token over a row of 16 blocks or more
 // takes 8-word slices (128 weights: the per-row scale, min and load work is
 // spread over twice the weights; the single-call kernel of q2k_m1.cu walks
-// such rows the same way, and the two must give the same bits); shorter rows
-// keep 4-word slices, so enough threads share each row.
+// such rows the same way, and the two must give the same bits), and so does
+// one q8_1 token over 8 to 15 blocks (the routed experts' down matrices:
+// the MoE step went from 25.8 to 22.8 us; bf16 rows of 8 blocks were slower
+// that way, 12.1 -> 13.4 us for the engram projection).  Shorter rows keep
+// 4-word slices, so enough threads share each row.  The choice depends on
+// the activation type, token count and row length alone, so an expert's row
+// and a single call give the same bits.
 int sw_for(int act, int m, int64_t nb)
 {
-    if (m == 1 && nb >= 16)
+    if (m == 1 && (nb >= 16 || (act == ACT_Q8 && nb >= 8)))
         return 8;
     if (act == ACT_Q8)
         return m <= 4 ? 4 : 2;

@@ -507,7 +507,7 @@ def test_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
 
 
 @pytest.mark.parametrize("n_mat,N,K,fused", [(160, 64, 256, False), (3, 4096, 2048, True), (24, 300, 1024, True),
-                                             (4, 200, 8192, True)])
+                                             (4, 200, 8192, True), (5, 700, 3840, True), (3, 333, 2304, False)])
 def test_experts_one_matrix_per_cta_equals_fused_sum(lib, n_mat, N, K, fused):
     """Per-matrix inputs with y given take one matrix per group of CTAs (more
     matrices than SMs: several waves) and a separate weighted sum; without y
@@ -530,6 +530,11 @@ def test_experts_one_matrix_per_cta_equals_fused_sum(lib, n_mat, N, K, fused):
         assert torch.equal(ys2, ysum)
     ref = (w.astype(np.float64)[:, None] * y.cpu().numpy().astype(np.float64)).sum(0)
     assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
+    # matrix 0's rows against the oracle (8-word slices from 8 blocks per row
+    # for one q8_1 token, 4-word below)
+    W0 = mats[0].cpu().numpy()
+    x0 = oracle.q8_1_dequant(xq[0:1].cpu().numpy(), 1, K)
+    assert rel_err_rows(y[0:1].cpu().numpy(), oracle.matvec(W0, N, K, x0)) <= 1e-4
 
 
 def test_experts_fused_sum_too_big_is_refused_before_any_launch(lib):
