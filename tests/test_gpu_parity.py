@@ -617,6 +617,46 @@ def test_moe_m1_cfg3(lib, cfg3):
     np.testing.assert_array_equal(ys.cpu().numpy(), y)
 
 
+def _moe_steps(lib, ptrs, E, dim, inter, x, w):
+    """The step run one call at a time: q8_1 of x, the gate/up batch, SwiGLU
+    + q8_1, the down batch with the route-weighted sum."""
+    xq = lib.q8_1_quantize_rows(x.view(1, dim))
+    gu, _ = lib.q2k_mmvq_experts(lib.pointer_table(ptrs[:2 * E]), inter, dim, xq)
+    hq, _ = lib.swiglu_q8_1_rows(gu)
+    ys = torch.empty(dim, dtype=torch.float32, device="cuda")
+    lib.q2k_mmvq_experts(lib.pointer_table(ptrs[2 * E:]), dim, inter, hq, x_per_matrix=True, route_w=w,
+                         y_sum=ys, want_y=False)
+    return ys
+
+
+# (E, dim, inter): both batches on 8-word slices (rows of 9 and 8 blocks, and
+# the configuration's 16 and 8), and on 4-word slices (rows of 4 and 2 blocks)
+@pytest.mark.parametrize("E,dim,inter", [(5, 2304, 2048), (8, 4096, 2048), (3, 1024, 512)])
+def test_moe_m1_equals_its_steps_and_the_oracle(lib, E, dim, inter):
+    gate = [synth.q2k_matrix(21, f"moe.g{E}.{e}", inter, dim) for e in range(E)]
+    up = [synth.q2k_matrix(21, f"moe.u{E}.{e}", inter, dim) for e in range(E)]
+    down = [synth.q2k_matrix(21, f"moe.d{E}.{e}", dim, inter) for e in range(E)]
+    ptrs = [dev(a) for a in gate + up + down]
+    tbl = lib.pointer_table(ptrs)
+    x = synth.bf16_normal(21, f"moe.x{E}", (1, dim))
+    w = np.random.default_rng(E).dirichlet(np.ones(E)).astype(np.float32)
+    xd, wd = bf16_dev(x[0]), dev(w)
+    steps = _moe_steps(lib, ptrs, E, dim, inter, xd, wd)
+    # a workspace holding garbage, the same workspace again, then x off a
+    # 16-byte boundary (its q8_1 in a launch of its own)
+    need = lib.q2k_moe_m1_workspace_bytes(E, dim, inter)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        y, _ = lib.q2k_moe_m1(tbl, E, dim, inter, xd, wd, workspace=ws)
+        assert torch.equal(y, steps)
+    xbuf = torch.zeros(dim + 8, dtype=torch.bfloat16, device="cuda")
+    xbuf[1:dim + 1] = xd
+    y2, _ = lib.q2k_moe_m1(tbl, E, dim, inter, xbuf[1:dim + 1], wd, workspace=ws)
+    assert torch.equal(y2, steps)
+    refq = oracle.moe_m1(x, gate, up, down, w, dim, inter, quantized=True)
+    assert rel_err_rows(y.cpu().numpy(), refq["y"]) <= 2e-3
+
+
 # ---- a7: dense GEMM -----------------------------------------------------------------
 
 @pytest.mark.parametrize("m,N,K,pad", [(1, 8, 16, 0), (3, 65, 64, 0), (16, 130, 200, 0), (17, 64, 1024, 0),
