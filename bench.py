@@ -26,8 +26,11 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   N=K=16384; small = one call of every other kernel at the configurations'
   shapes; q3k = the Q3_K MMVQ at m=1 and 2; mmq = the Q2_K matmul for many
   tokens at m=64 and m=256, N=K=16384; moe = the MoE step on 8 experts.
-* --all also times every configuration of the sweep and prints one JSON
-  object per configuration to stderr (and to the file --all-out names).
+* After the headline (one GPU) every configuration of the sweep is timed
+  with 300 calls each and added to the JSON line as configs_measured, with
+  its own clock record (--no-configs skips it).  --all times them with 2000
+  calls each and prints one JSON object per configuration to stderr (and to
+  the file --all-out names).
 With torchrun (N > 1) every rank runs an independent replica (the path is
 replicated, not sharded); value = all ranks' bytes / the slowest rank's time.
 """
@@ -328,8 +331,28 @@ def run_ours(args):
             "parity_max_rel_err_sampled": parity_err,
             "cpu_baseline": cpu,
         }
-    if args.all:
-        sweep(q, L, l2, hbm, rank, args.all_out)
+    if args.all or (ws == 1 and not args.no_configs):
+        # every configuration, timed in this run after the headline (fewer
+        # calls each unless --all); clocks sampled across it
+        scale = 1.0 if args.all else 0.15
+        sampler = ClockSampler(gpu_id)
+        sampler.start()
+        try:
+            recs, err = sweep(q, L, l2, hbm, rank, args.all_out, scale=scale), None
+        except Exception as ex:  # the headline line goes out whatever happens here
+            recs, err = [], f"{type(ex).__name__}: {ex}"
+        ck2 = sampler.stop()
+        if line is not None:
+            line["configs_measured"] = {
+                "what": "every configuration of the sweep, timed in this process after the headline: CUDA graphs "
+                        "of C-ABI calls, weights cycled past L2, us per call and fraction of the measured HBM peak",
+                "calls_per_config": f"{max(100, int(2000 * scale))} (graphs of 100)",
+                "clocks": ck2,
+                "rows": {r["config"]: {"us_per_call": round(r["us_per_call"], 3), "frac_hbm": round(r["frac_hbm"], 4)}
+                         for r in recs},
+            }
+            if err:
+                line["configs_measured"]["error"] = err
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -393,9 +416,15 @@ def cpu_baseline(W, x, budget_s: float = 10.0):
 
 # ---- sweep over every configuration (--all) ------------------------------------------------
 
-def sweep(q, L, l2, hbm, rank, all_out=None):
+def sweep(q, L, l2, hbm, rank, all_out=None, scale=1.0):
+    """Time every configuration of the sweep (graphs of C-ABI calls, weights
+    cycled past L2); scale < 1 times fewer calls per configuration.  Returns
+    the records."""
     import torch
     out = []
+
+    def gt(launch, steps, warmup):
+        return graph_time(launch, max(100, int(steps * scale)), max(10, int(warmup * scale)))
 
     def rec(name, t_call, nbytes, m, extra=None):
         d = {"config": name, "us_per_call": t_call * 1e6, "bytes_per_call": int(nbytes),
@@ -427,10 +456,10 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
             xq = q.q8_1_quantize_rows(xd)
             y = torch.empty((m, N), dtype=torch.float32, device="cuda")
             nb = W.nbytes
-            el, n = graph_time(lambda i: check(L.q2k_gemv_bf16(wp[i % R], N, K, P(xd), m, K, P(y), N, cur()), "gemv"),
+            el, n = gt(lambda i: check(L.q2k_gemv_bf16(wp[i % R], N, K, P(xd), m, K, P(y), N, cur()), "gemv"),
                                2000, 100)
             rec(f"gemv_bf16 N={N} K={K} m={m}", el / n, nb + 2 * m * K + 4 * m * N, m)
-            el, n = graph_time(lambda i: check(L.q2k_mmvq_q8_1(wp[i % R], N, K, P(xq), m, P(y), N, cur()), "mmvq"),
+            el, n = gt(lambda i: check(L.q2k_mmvq_q8_1(wp[i % R], N, K, P(xq), m, P(y), N, cur()), "mmvq"),
                                2000, 100)
             rec(f"mmvq_q8_1 N={N} K={K} m={m}", el / n, nb + xq.numel() + 4 * m * N, m)
         del Ws, W0
@@ -453,13 +482,13 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         def pair(i):
             check(L.q8_1_quantize_rows(P(xd), m, K, K, P(xq), cur()), "q8")
             check(L.q2k_mmvq_pair(P(Was[i % R]), 1024, P(ya), P(Wbs[i % R]), 512, P(yb), K, P(xq), m, cur()), "pair")
-        el, n = graph_time(pair, 2000, 100)
+        el, n = gt(pair, 2000, 100)
         rec(f"pair (q8_1 + wq_a/wkv) m={m}", el / n, Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
         # the same as one call from bf16 (the q8_1 encoding inside the pair launch for m = 1)
         def pair_bf16(i):
             check(L.q2k_mmvq_pair_bf16(P(Was[i % R]), 1024, P(ya), P(Wbs[i % R]), 512, P(yb), K, P(xd), m, P(xq),
                                        cur()), "pair_bf16")
-        el, n = graph_time(pair_bf16, 2000, 100)
+        el, n = gt(pair_bf16, 2000, 100)
         rec(f"pair from bf16 (q8_1 inside the call) m={m}", el / n,
             Wa.nbytes + Wb.nbytes + xq.numel() + 2 * m * K + 4 * m * 1536, m)
     del Was, Wbs
@@ -474,7 +503,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
         xq = q.q8_1_quantize_rows(xd)
         yg = torch.empty((m, G * Rg), dtype=torch.float32, device="cuda")
-        el, n = graph_time(lambda i: check(L.q2k_mmvq_grouped(P(Wgs[i % R]), G, Rg, Kg, P(xq), m, P(yg), cur()),
+        el, n = gt(lambda i: check(L.q2k_mmvq_grouped(P(Wgs[i % R]), G, Rg, Kg, P(xq), m, P(yg), cur()),
                                            "grouped"), 2000, 100)
         rec(f"grouped wo_a MMVQ {G}x[{Rg},{Kg}] m={m}", el / n, Wg.nbytes + xq.numel() + 4 * m * G * Rg, m)
     del Wgs
@@ -491,7 +520,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
             xq = q.q8_1_quantize_rows(torch.from_numpy(synth.bf16_normal(0, f"sweep.q3.x{m}", (m, K)).view(np.int16))
                                       .cuda().view(torch.bfloat16))
             y = torch.empty((m, N), dtype=torch.float32, device="cuda")
-            el, n = graph_time(lambda i: check(L.q3k_mmvq_q8_1(P(W3s[i % R]), N, K, P(xq), m, P(y), N, cur()),
+            el, n = gt(lambda i: check(L.q3k_mmvq_q8_1(P(W3s[i % R]), N, K, P(xq), m, P(y), N, cur()),
                                                "q3k"), 2000, 100)
             rec(f"q3k mmvq_q8_1 N={N} K={K} m={m}", el / n, W3.nbytes + xq.numel() + 4 * m * N, m)
         del W3s, W30
@@ -516,10 +545,10 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     ys = torch.empty(dim, dtype=torch.float32, device="cuda")
     wd = torch.from_numpy(synth.expert_route(0, 256, topk)[1]).cuda()
     mb = inter * (dim // 256) * 110
-    el, n = graph_time(lambda i: check(L.q3k_mmvq_experts(P(gu_t[i % 32]), 2 * topk, inter, dim, P(xq), 0, P(y_gu),
+    el, n = gt(lambda i: check(L.q3k_mmvq_experts(P(gu_t[i % 32]), 2 * topk, inter, dim, P(xq), 0, P(y_gu),
                                                           None, None, cur()), "q3k_ex"), 1000, 50)
     rec("q3k experts gate/up batch 16x[2048,4096] m=1", el / n, 2 * topk * mb, 1)
-    el, n = graph_time(lambda i: check(L.q3k_mmvq_experts(P(dn_t[i % 32]), topk, dim, inter, P(hq), 1, P(y_dn),
+    el, n = gt(lambda i: check(L.q3k_mmvq_experts(P(dn_t[i % 32]), topk, dim, inter, P(hq), 1, P(y_dn),
                                                           P(wd), P(ys), cur()), "q3k_ex"), 1000, 50)
     rec("q3k experts down batch 8x[4096,2048] + weighted sum", el / n, topk * mb, 1, {"launches_per_call": 2})
     del q3, gu_t, dn_t
@@ -544,7 +573,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     yo = torch.empty(dim, dtype=torch.float32, device="cuda")
     wsb = q.q2k_moe_m1_workspace_bytes(topk, dim, inter)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    el, n = graph_time(lambda i: check(L.q2k_moe_m1(P(tables[i % 64]), topk, dim, inter, P(xd), P(wd), P(yo), P(ws),
+    el, n = gt(lambda i: check(L.q2k_moe_m1(P(tables[i % 64]), topk, dim, inter, P(xd), P(wd), P(yo), P(ws),
                                                     wsb, cur()), "moe"), 1000, 50)
     moe_bytes = 3 * topk * inter * (dim // 256) * 84
     rec("moe_m1 (8 of 256 experts, gate/up -> SwiGLU -> down)", el / n, moe_bytes, 1, {"launches_per_call": 3})
@@ -564,7 +593,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     def engram(i):
         check(L.q2k_dequant_rows(P(table), n_table, 256, P(ids), 128, P(rows), None, cur()), "dequant")
         check(L.dense_gemm_bf16(P(rows), 16, 2048, 2048, P(wkvs[i % R]), 20480, P(yk), 20480, cur()), "gemm")
-    el, n = graph_time(engram, 500, 20)
+    el, n = gt(engram, 500, 20)
     rec("engram rows(128) + dense_gemm m=16 [20480x2048]", el / n, wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 +
         16 * 20480 * 4, 16)
 
@@ -585,7 +614,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
                                 P(offs), 0, P(hout), P(lids), 1, None, cur()), "hash")
         check(L.q2k_dequant_rows(P(table), n_table, 256, P(lids), 128, P(rows), None, cur()), "dequant")
         check(L.dense_gemm_bf16(P(rows), 16, 2048, 2048, P(wkvs[i % R]), 20480, P(yk), 20480, cur()), "gemm")
-    el, n = graph_time(engram_chain, 500, 20)
+    el, n = gt(engram_chain, 500, 20)
     rec("engram hash(16 tok) + rows(128) + dense_gemm m=16 [20480x2048]", el / n,
         wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 + 16 * 20480 * 4, 16)
     del wkvs
@@ -606,7 +635,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
                                 P(offs), 0, P(hout1), P(lids1), 1, None, cur()), "hash")
         check(L.q2k_dequant_rows(P(table), n_table, 256, P(lids1), 8, P(rows1), None, cur()), "dequant")
         check(L.q2k_gemv_bf16(P(wqs[i % R]), 20480, 2048, P(rows1), 1, 2048, P(y1), 20480, cur()), "gemv")
-    el, n = graph_time(engram_one, 2000, 100)
+    el, n = gt(engram_one, 2000, 100)
     rec("engram one token: hash + rows(8) + q2k_gemv_bf16 [20480x2048] (wkv_q2k)", el / n,
         wq.nbytes + 8 * 84 + 2 * 8 * 256 * 2 + 20480 * 4, 1, {"launches_per_call": 3})
 
@@ -619,7 +648,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     def engram_step_one(i):
         engram_one(i)
         check(L.q2k_engram_gate(P(st1), P(y1), 20480, P(qk), 1, 4, 4096, ctypes.c_float(1e-6), None, cur()), "gate")
-    el, n = graph_time(engram_step_one, 2000, 100)
+    el, n = gt(engram_step_one, 2000, 100)
     rec("engram step one token: hash + rows(8) + q2k_gemv_bf16 (wkv_q2k) + gate [4x4096]", el / n,
         wq.nbytes + 8 * 84 + 2 * 8 * 256 * 2 + 20480 * 4 + 20480 * 4 + 3 * 4 * 4096 * 4, 1, {"launches_per_call": 4})
     del wqs
@@ -629,7 +658,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
     def engram_step16(i):
         engram_chain(i)
         check(L.q2k_engram_gate(P(st16), P(yk), 20480, P(qk), 16, 4, 4096, ctypes.c_float(1e-6), None, cur()), "gate")
-    el, n = graph_time(engram_step16, 500, 20)
+    el, n = gt(engram_step16, 500, 20)
     rec("engram step 16 tokens: hash + rows(128) + dense_gemm m=16 + gate [16x4x4096]", el / n,
         wkv.nbytes + 128 * 84 + 2 * 128 * 256 * 2 + 16 * 20480 * 4 * 2 + 16 * 3 * 4 * 4096 * 4, 16,
         {"launches_per_call": 4})
@@ -643,7 +672,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         for m in (64, 256):
             xx = torch.from_numpy(synth.bf16_normal(0, f"sweep.dense.x{m}.{Nn}", (m, Nn)).view(np.int16)).cuda()
             yy = torch.empty((m, Nn), dtype=torch.float32, device="cuda")
-            el, n = graph_time(lambda i: check(L.dense_gemm_bf16(P(xx), m, Nn, Nn, P(Wds[i % R]), Nn, P(yy), Nn, cur()),
+            el, n = gt(lambda i: check(L.dense_gemm_bf16(P(xx), m, Nn, Nn, P(Wds[i % R]), Nn, P(yy), Nn, cur()),
                                                "gemm"), 200, 10)
             flops = 2.0 * m * Nn * Nn
             rec(f"dense_gemm_bf16 m={m} N=K={Nn}", el / n, Wdn.nbytes + 2 * m * Nn + 4 * m * Nn, m,
@@ -659,14 +688,14 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         for m in (64, 256):
             xx = torch.from_numpy(synth.bf16_normal(0, f"sweep.dense.x{m}.{Nn}", (m, Nn)).view(np.int16)).cuda()
             yy = torch.empty((m, Nn), dtype=torch.float32, device="cuda")
-            el, n = graph_time(lambda i: check(L.q2k_mmq_bf16(P(Wqs[i % R]), Nn, Nn, P(xx), m, Nn, P(yy), Nn, cur()),
+            el, n = gt(lambda i: check(L.q2k_mmq_bf16(P(Wqs[i % R]), Nn, Nn, P(xx), m, Nn, P(yy), Nn, cur()),
                                                "mmq"), 200, 10)
             flops = 2.0 * m * Nn * Nn
             rec(f"q2k_mmq_bf16 m={m} N=K={Nn}", el / n, Wq.nbytes + 2 * m * Nn + 4 * m * Nn, m,
                 {"TFLOPs": flops / (el / n) / 1e12})
             xq = q.q8_1_quantize_rows(xx.view(torch.bfloat16))
             ws = torch.empty(q.q2k_mmq_q8_1_workspace_bytes(m, Nn), dtype=torch.uint8, device="cuda")
-            el, n = graph_time(lambda i: check(L.q2k_mmq_q8_1(P(Wqs[i % R]), Nn, Nn, P(xq), m, P(yy), Nn, P(ws),
+            el, n = gt(lambda i: check(L.q2k_mmq_q8_1(P(Wqs[i % R]), Nn, Nn, P(xq), m, P(yy), Nn, P(ws),
                                                               ws.numel(), cur()), "mmq8"), 200, 10)
             rec(f"q2k_mmq_q8_1 m={m} N=K={Nn}", el / n, Wq.nbytes + xq.numel() + 4 * m * Nn, m,
                 {"TFLOPs": flops / (el / n) / 1e12, "launches_per_call": 2})
@@ -677,6 +706,7 @@ def sweep(q, L, l2, hbm, rank, all_out=None):
         with open(all_out, "w") as f:
             for d in out:
                 f.write(json.dumps(d) + "\n")
+    return out
 
 
 # ---- reference arm: the CPU oracle -------------------------------------------------------------
@@ -841,6 +871,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true")
     ap.add_argument("--all-out", default=None, help="also write the --all records here, one JSON object a line")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other configurations after the headline")
     ap.add_argument("--ncu-case", nargs="?", const="mv", choices=["mv", "mt", "gemm", "small", "q3k", "mmq", "moe"], default=None)
     args = ap.parse_args(argv)
     if args.ncu_case:
