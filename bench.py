@@ -26,9 +26,9 @@ against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
   N=K=16384; small = one call of every other kernel at the configurations'
   shapes; q3k = the Q3_K MMVQ at m=1 and 2; mmq = the Q2_K matmul for many
   tokens at m=64 and m=256, N=K=16384; moe = the MoE step on 8 experts.
-* After the headline (one GPU) every configuration of the sweep is timed
-  with 300 calls each and added to the JSON line as configs_measured, with
-  its own clock record (--no-configs skips it).  --all times them with 2000
+* After the headline (one GPU, --steps 1000 or more) every configuration of
+  the sweep is timed with 300 calls each and added to the JSON line as
+  configs_measured, with its own clock record (--no-configs skips it).  --all times them with 2000
   calls each and prints one JSON object per configuration to stderr (and to
   the file --all-out names).
 With torchrun (N > 1) every rank runs an independent replica (the path is
@@ -331,9 +331,11 @@ def run_ours(args):
             "parity_max_rel_err_sampled": parity_err,
             "cpu_baseline": cpu,
         }
-    if args.all or (ws == 1 and not args.no_configs):
+    if args.all or (ws == 1 and not args.no_configs and args.steps >= 1000):
         # every configuration, timed in this run after the headline (fewer
-        # calls each unless --all); clocks sampled across it
+        # calls each unless --all); clocks sampled across it.  Short runs
+        # (profiler captures) leave it out, so their launches are the
+        # headline's alone.
         scale = 1.0 if args.all else 0.15
         sampler = ClockSampler(gpu_id)
         sampler.start()
