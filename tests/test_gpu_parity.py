@@ -480,6 +480,25 @@ def test_grouped_mmvq(lib, groups, R, Kg, m):
             np.testing.assert_array_equal(y[:, g * R:(g + 1) * R], single)
 
 
+@pytest.mark.parametrize("m,act", [(3, "bf16"), (8, "q8_1")])
+def test_tensor_core_mmvq_in_waves(lib, m, act):
+    """1537 row tiles: more than eight per CTA on one CTA per SM, so the
+    tensor-core MMVQ runs more CTAs than SMs, in waves; a ragged last tile."""
+    N, K = 24577, 2048
+    W = synth.q2k_matrix(14, "mt.waves", N, K)
+    x = synth.bf16_normal(14, f"mt.waves.x{m}", (m, K))
+    rows = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 40, N)]))
+    Ws = np.ascontiguousarray(W[rows])
+    if act == "bf16":
+        y = lib.q2k_gemv_bf16(dev(W), bf16_dev(x)).cpu().numpy()
+        assert rel_err_rows(y[:, rows], oracle.matvec(Ws, len(rows), K, x_f64(x))) <= TOL_BF16
+    else:
+        xq = lib.q8_1_quantize_rows(bf16_dev(x))
+        y = lib.q2k_mmvq_q8_1(dev(W), xq, K).cpu().numpy()
+        ref = oracle.matvec(Ws, len(rows), K, oracle.q8_1_dequant(xq.cpu().numpy(), m, K))
+        assert rel_err_rows(y[:, rows], ref) <= 1e-4
+
+
 # ---- a6: routed experts -------------------------------------------------------------
 
 @pytest.mark.parametrize("per_matrix", [False, True])

@@ -130,6 +130,20 @@ def test_q3k_mmvq_output_stride_leaves_the_gap(lib):
     assert (out[:, N:] == 7.0).all()
 
 
+@pytest.mark.parametrize("m", [3, 8])
+def test_q3k_several_tokens_in_waves(lib, m):
+    # 1537 row tiles: more than eight per CTA on one CTA per SM, so the
+    # tensor-core kernel runs more CTAs than SMs, in waves; a ragged last tile
+    N, K = 24577, 2048
+    W = synth.q3k_matrix(13, "q3.waves", N, K)
+    x = synth.bf16_normal(13, f"q3.waves.x{m}", (m, K))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q3k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 40, N)]))
+    ref = oracle.q3k_matvec(np.ascontiguousarray(W[rows]), len(rows), K, oracle.q8_1_dequant(xq, m, K))
+    assert rel_err_rows(y[:, rows], ref) <= TOL_EXACT_X
+
+
 @pytest.fixture(scope="module")
 def big_w3():
     W = synth.q3k_matrix(0, "q3.W16384", 16384, 16384)
