@@ -348,7 +348,7 @@ int q2k_moe_m1_static_scratch(const void* const* ptrs, int64_t E, int64_t dim, i
  * once per call too and are the faster route.  When the library splits K
  * across thread blocks (few weight tiles), partial sums are added with fp32
  * atomics, so the last bits may differ between runs.
- * Q2K_ERR_UNSUPPORTED when the driver offers no tensor-map encoder. */
+ * Q2K_ERR_UNSUPPORTED when the CUDA driver offers no tensor-map encoder. */
 int q2k_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx, float* y,
                  int64_t ldy, q2k_stream_t stream);
 
