@@ -58,12 +58,14 @@ cudaError_t launch_mv(const MvProblem& p, cudaStream_t s);
 // device (shared memory for the ring and the partial sums); no CUDA call
 // besides the cached device query.
 bool mv_plan_ok(const MvProblem& p);
-// One token (bf16 or q8_1), two tokens, or four q8_1 tokens over rows of
-// 32..128 blocks (K % 1024 == 0, 16-byte aligned weights and activations),
-// one or two explicit segments: row teams fed by ~43 KB stages (q2k_m1.cu).
+// One token (bf16 or q8_1) over rows of 16..128 blocks, or two tokens, or
+// four q8_1 tokens over rows of 8..128 blocks (K % 1024 == 0, 16-byte
+// aligned weights and activations), one or two explicit segments: row teams
+// fed by ~43 KB stages (q2k_m1.cu).
 bool m1_supported(const MvProblem& p);
 cudaError_t launch_m1(const MvProblem& p, cudaStream_t s);
-// Several tokens (m = 2..8, explicit segments) on the tensor cores.
+// Several tokens (bf16 m = 3..8, q8_1 m = 5..8; explicit segments) on the
+// tensor cores (q2k_mt.cu).
 bool mt_supported(const MvProblem& p);
 cudaError_t launch_mt(const MvProblem& p, cudaStream_t s);
 
