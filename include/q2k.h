@@ -162,16 +162,21 @@ int q8_1_quantize_rows(const uint16_t* x_bf16, int64_t m, int64_t K, int64_t ldx
 /* Q2_K GEMV with bf16 activations, m = 1..8 tokens (engram_v41/apply.rs,
  * the single-token `engram_v41_wkv_q2k_gemv` off `wkv_q2k`).
  *   W  Q2_K [N, K];  x  bf16 [m, K], row stride ldx;  y  fp32 [m, N], row
- *   stride ldy.  y[t, n] = sum_k w[n, k] x[t, k]: exact int32 dot products
- *   of the 2-bit codes with fixed-point activations per sub-block, scaled
- *   by d, the sub-block scales and the activation exponents and summed in
- *   fp32 (the bf16 values are not multiplied as floats).
+ *   stride ldy.  y[t, n] = sum_k w[n, k] x[t, k].  One and two tokens:
+ *   exact int32 dot products of the 2-bit codes with fixed-point
+ *   activations per sub-block, scaled by d, the sub-block scales and the
+ *   activation exponents and summed in fp32 (the bf16 values are not
+ *   multiplied as floats).
  * The activations enter the integer dot products as 16-bit fixed point
  * with one power-of-two exponent per 16 values (exact unless a group spans
  * more than 2^7 in magnitude; then the smallest lose bits below 2^-15 of
  * the group maximum).  One token over rows of K >= 4096 uses one exponent
  * per 32 values and a 2^14 range (exact within 2^6 of the group maximum,
- * bits below 2^-14 of it lost).  Groups below 2^-100 count as zero. */
+ * bits below 2^-14 of it lost).  Groups below 2^-100 count as zero.
+ * Three to eight tokens run on the tensor cores instead: the bf16 values
+ * enter exactly, against the integers 128 + sc*q of each sub-block (fp32
+ * accumulation), and the min term's sub-block sums of x enter as a bf16
+ * high and low pair. */
 int q2k_gemv_bf16(const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t m, int64_t ldx,
                   float* y, int64_t ldy, q2k_stream_t stream);
 
