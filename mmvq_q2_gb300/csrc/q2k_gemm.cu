@@ -161,17 +161,10 @@ cudaError_t launch_bt(const uint16_t* x, int m, int K, int64_t ldx, const uint16
                       int sm_count, cudaStream_t s)
 {
     constexpr int SMEM = kStages * (kBN * kBK * 2 + BT * kBK * 2);
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<unsigned long long> smem_devs{0};
+    cudaError_t e = allow_max_smem(dense_gemm_kernel<BT>, smem_devs);
     if (e != cudaSuccess)
         return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(dense_gemm_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess)
-            return e;
-        configured_dev = dev;
-    }
     const int gx = (N + kBN - 1) / kBN;
     const int gy = (m + BT - 1) / BT;
     const int nkt = (K + kBK - 1) / kBK;

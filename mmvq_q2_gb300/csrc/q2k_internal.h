@@ -5,9 +5,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace q2k {
 
 enum Act : int { ACT_BF16 = 0, ACT_Q8 = 1 };
+
+// Let `kernel` take up to the device's opt-in shared memory per block, once
+// per device (devs: a bit per device id below 64 that has it).  The limit
+// is only ever raised to that maximum, so concurrent callers with different
+// needs cannot lower it under one another; a repeated first call is
+// harmless.
+template <typename Kernel>
+inline cudaError_t allow_max_smem(Kernel kernel, std::atomic<unsigned long long>& devs)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (devs.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    int optin = 0;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)) != cudaSuccess)
+        return e;
+    devs.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
 
 // Per-device facts read once (multiprocessor count, shared memory limit).
 struct DeviceInfo {

@@ -576,16 +576,9 @@ cudaError_t launch_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t*
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    static int configured_dev = -1;
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess)
+    static std::atomic<unsigned long long> smem_devs{0};
+    if ((e = allow_max_smem(q2k_mmq_kernel, smem_devs)) != cudaSuccess)
         return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(q2k_mmq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(227 * 1024));
-        if (e != cudaSuccess)
-            return e;
-        configured_dev = dev;
-    }
     if (a.atomic) {
         e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), (size_t)m, s);
         if (e != cudaSuccess)

@@ -675,19 +675,10 @@ cudaError_t launch_mt_one(const MtArgs& a, const CUtensorMap& tm0, const CUtenso
                           cudaStream_t s)
 {
     auto k = q2k_mt_kernel<ACT>;
-    static int configured_for = -1;
-    static size_t configured_smem = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<unsigned long long> smem_devs{0};
+    cudaError_t e = allow_max_smem(k, smem_devs);
     if (e != cudaSuccess)
         return e;
-    if (configured_for != dev || configured_smem < smem) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured_for = dev;
-        configured_smem = smem;
-    }
     return launch_pdl(k, dim3((unsigned)grid), dim3(kMtThreads), smem, s, a, tm0, tm1);
 }
 

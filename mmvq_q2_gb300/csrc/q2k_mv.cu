@@ -614,19 +614,10 @@ template <int M, int ACT, int SW>
 cudaError_t launch_one(const MvArgs& a, int grid, size_t smem, cudaStream_t s)
 {
     auto k = q2k_mv_kernel<M, ACT, SW>;
-    static int configured_for = -1;  // device id the attribute was set for
-    static size_t configured_smem = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<unsigned long long> smem_devs{0};
+    cudaError_t e = allow_max_smem(k, smem_devs);
     if (e != cudaSuccess)
         return e;
-    if (configured_for != dev || configured_smem < smem) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured_for = dev;
-        configured_smem = smem;
-    }
     return launch_pdl(k, dim3((unsigned)grid), dim3((unsigned)a.tc), smem, s, a);
 }
 

@@ -258,16 +258,9 @@ cudaError_t launch_dense_gemm_tc(const uint16_t* x, int64_t m, int64_t K, int64_
     CUtensorMap tw{}, tx{};
     if (!encode_bf16(&tw, W, N, K, K, kBM) || !encode_bf16(&tx, x, m, K, ldx, a.ntok))
         return cudaErrorInvalidValue;
-    static int configured_dev = -1;
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess)
+    static std::atomic<unsigned long long> smem_devs{0};
+    if ((e = allow_max_smem(umma_gemm_kernel, smem_devs)) != cudaSuccess)
         return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(224 * 1024));
-        if (e != cudaSuccess)
-            return e;
-        configured_dev = dev;
-    }
     if (a.atomic) {
         e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), (size_t)m, s);
         if (e != cudaSuccess)

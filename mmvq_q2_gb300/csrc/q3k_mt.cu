@@ -605,19 +605,9 @@ cudaError_t launch_q3k_mt(const Q3Problem& p, cudaStream_t s)
     CUtensorMap tm{};
     if (a.w_tma && !encode_q3_rows(&tm, a.W, a.N, a.row_bytes))
         a.w_tma = 0;  // the warp-copy path
-    static int configured_for = -1;
-    static size_t configured_smem = 0;
-    int dev = 0;
-    err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
+    static std::atomic<unsigned long long> smem_devs{0};
+    if ((err = allow_max_smem(q3k_mt_kernel, smem_devs)) != cudaSuccess)
         return err;
-    if (configured_for != dev || configured_smem < smem) {
-        err = cudaFuncSetAttribute(q3k_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess)
-            return err;
-        configured_for = dev;
-        configured_smem = smem;
-    }
     return launch_pdl(q3k_mt_kernel, dim3((unsigned)grid), dim3(kQtThreads), smem, s, a, tm);
 }
 
