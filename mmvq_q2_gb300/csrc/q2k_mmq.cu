@@ -27,10 +27,12 @@
 //                add it into y while the next one fills (two accumulators
 //                when the token tile is at most 128 wide).
 // Measured on this GPU, and the reasons for the shape:
-//   * a tcgen05.mma of M = 128, K = 16 costs about 128 cycles for any N up
-//     to 256, so one token tile of up to 256 serves every token count up to
-//     256, and the expansion goes to tensor memory (its stores do not
-//     compete with the MMA's operand reads in shared memory);
+//   * the tensor work of a tcgen05.mma of M = 128, K = 16 is about N/2
+//     cycles (128 at N = 256), while one thread issuing alone spends about
+//     50 cycles per MMA: narrow token tiles gain little, so one token tile
+//     of up to 256 serves every token count up to 256, and the expansion
+//     goes to tensor memory (its stores do not compete with the MMA's
+//     operand reads in shared memory);
 //   * the issuing thread's own mbarrier waits, commits and MMA issues cost
 //     about 100, 70 and 64 cycles each, even when nothing is pending.  So a
 //     stage is 128 K (8 MMAs) behind ONE barrier: "full" completes when the
