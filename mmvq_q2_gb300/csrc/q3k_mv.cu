@@ -394,6 +394,291 @@ int q3_lw(int mg, int nb)
     return lw;
 }
 
+// ---- one token over long rows: row teams over a ring of whole rows ----
+//
+// The design of the Q2_K one-token kernel (q2k_m1.cu) with Q3_K blocks.
+// One CTA of 16 warps per SM owns a contiguous range of rows.  A row team
+// has two lanes per block column, each with the 16-byte-position slice
+// (128 weights) that read_slice / dot_slice take, so every lane keeps its
+// q8_1 activations in registers for every row it visits.  Whole rows arrive
+// by 1-D bulk copies into a ring of stages (two rows per team a stage); the
+// warp last out of a stage refills its slot one stage later.  A lane's
+// partial, the warp's butterfly sum (xor 16, 8, 4, 2, 1) and the sum of the
+// team's warps in warp order are the same operations, in the same order,
+// as q3k_mv_kernel<1, 16> performs (its warp covers the same 16 block
+// columns), so both give the same bits: the expert batches, which run
+// there, keep equal to single calls.
+constexpr int kQm1Threads = 512;
+constexpr int kQm1Warps = kQm1Threads / 32;
+constexpr int kQm1Lw = 16;   // byte positions per lane: 128 weights of a block
+constexpr int kQm1Rps = 2;   // rows per team in a stage
+constexpr int kQm1Rows = 4;  // rows per lane between two warp reductions (two stages)
+
+struct Qm1Args {
+    const uint8_t* W;
+    float* y;
+    const uint8_t* x;  // one q8_1 row
+    int nb;
+    int lanes;         // lanes per row team: a power of two >= 2 * nb, 32..256
+    int log_lanes;
+    int teams;         // kQm1Threads / lanes
+    int wpt;           // warps per team
+    int depth;         // stages in the ring
+    int rows_q, rows_r;  // CTA c owns rows_q rows (+1 if c < rows_r)
+    uint32_t row_bytes, stage_bytes, x_bytes;
+    uint32_t off_x, off_bar, off_red;
+};
+
+// The warp sums of v[0..3]: lane L returns the sum of v[L >> 3] over the
+// warp, paired as a butterfly over lane bits 4, 3, 2, 1, 0.
+__device__ __forceinline__ float reduce4_rows(const float (&v)[4], int lane)
+{
+    const bool up = (lane & 16) != 0;
+    float a0 = up ? v[2] : v[0], a1 = up ? v[3] : v[1];
+    const float b0 = up ? v[0] : v[2], b1 = up ? v[1] : v[3];
+    a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
+    const bool u8 = (lane & 8) != 0;
+    float c = u8 ? a1 : a0;
+    const float e = u8 ? a0 : a1;
+    c += __shfl_xor_sync(0xffffffffu, e, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+}
+
+__global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int WPL = kQm1Lw / 4;
+    pdl_launch_dependents();  // the next kernel may set itself up meanwhile
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int team = tid >> a.log_lanes;
+    const int li = tid & (a.lanes - 1);  // lane within the team
+    const int wit = li >> 5;             // warp within the team: the chunk of 16 block columns
+
+    uint8_t* ring = smem;
+    const uint8_t* xsm = smem + a.off_x;
+    uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+    uint64_t* xbar = full_b + a.depth;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xbar + 1);
+    int* released = reinterpret_cast<int*>(xbar + 2);  // per slot: warps done, over all its stages
+    int* uses = released + a.depth;                      // per slot: copies requested
+    float* red = reinterpret_cast<float*>(smem + a.off_red);
+
+    const int cta = (int)blockIdx.x;
+    const int lo = cta * a.rows_q + min(cta, a.rows_r);
+    const int hi = lo + a.rows_q + (cta < a.rows_r ? 1 : 0);
+    const int spr = kQm1Rps * a.teams;          // rows per stage
+    const int nst = (hi - lo + spr - 1) / spr;  // stage j: rows lo + spr*j + kQm1Rps*team + q
+
+    if (tid == 0) {
+        mbar_init(smem_u32(xbar), 1);
+        *abort_flag = 0;
+    }
+    if (tid < a.depth) {
+        mbar_init(smem_u32(&full_b[tid]), 1);
+        released[tid] = 0;
+        uses[tid] = 0;
+    }
+    fence_mbar_init();
+    __syncthreads();
+    // nothing above touched global memory
+    pdl_wait();
+
+    // stage j into slot s (one thread): the stage's rows, one bulk copy
+    auto issue = [&](int j, int s) {
+        const int r0 = lo + spr * j;
+        const int r1 = min(hi, r0 + spr);
+        const uint32_t fb = smem_u32(&full_b[s]);
+        const uint32_t bytes = (uint32_t)(r1 - r0) * a.row_bytes;
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_copy_g2s_hint(smem_u32(ring + (size_t)s * a.stage_bytes), a.W + (int64_t)r0 * a.row_bytes, bytes, fb,
+                           l2_policy_evict_first());
+        atomicAdd(&uses[s], 1);
+    };
+    if (tid == 0) {
+        // the activations first (every CTA reads them: keep them in L2), then
+        // the whole ring
+        mbar_arrive_expect_tx(smem_u32(xbar), a.x_bytes);
+        bulk_copy_g2s_hint(smem_u32(smem + a.off_x), a.x, a.x_bytes, smem_u32(xbar), l2_policy_evict_last());
+        for (int j = 0; j < min(a.depth, nst); ++j)
+            issue(j, j);
+    }
+    // every lane waits for itself; gives up after about two seconds
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (mbar_wait_bounded(bar, parity, abort_flag))
+            return true;
+        atomicOr(&g_q3_error, Q2K_ERR_BIT_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+    };
+
+    // this lane's slice: block column b, byte positions l0 .. l0 + 15
+    const bool active = li < 2 * a.nb;
+    const int b = active ? li >> 1 : 0;
+    const int l0 = (li & 1) * kQm1Lw;
+    const uint32_t lsel = l0 ? 0x7531u : 0x6420u;
+    const uint32_t hsel = l0 ? 0x3131u : 0x2020u;
+    bool aborted = !wait(smem_u32(xbar), 0);
+    // q8_1 blocks 8b + 4n + j: d8, the lane's 16 q8 bytes, and the start of
+    // the (n, j) chain, -4 * 4^j * (their sum) (16 for j = 3)
+    uint32_t xq[1][8][WPL];
+    float d8[1][8];
+    int c4[1][8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint8_t* xb = xsm + ((size_t)b * 8 + k) * kQ8Bytes;
+        d8[0][k] = active ? half_lo_f(lds32(xb)) : 0.f;
+        int sq = 0;
+#pragma unroll
+        for (int w = 0; w < WPL; ++w) {
+            xq[0][k][w] = active ? lds32(xb + 4 + l0 + 4 * w) : 0u;
+            sq = dp4a_us(0x01010101u, xq[0][k][w], sq);
+        }
+        const int j = k & 3;
+        c4[0][k] = -4 * sq * (j < 3 ? (1 << (2 * j)) : 16);
+    }
+
+    const uint8_t* blk0 = ring + (size_t)team * kQm1Rps * a.row_bytes + (size_t)b * kQ3Bytes;
+    // stage j's slot and the parity of its phase there, advanced one stage
+    // at a time; the previous stage (its slot, and the count the last warp
+    // out of it sees) and, in lane 0, what this warp's atomic returned
+    int s = 0, kd = 0;
+    uint32_t parity = 0;
+    int prev_j = -1, prev_s = 0, prev_last = 0, prev_count = 0;
+    auto stage = [&](int j, float* v) {
+        if (!aborted && !wait(smem_u32(&full_b[s]), parity))
+            aborted = true;
+#pragma unroll
+        for (int q = 0; q < kQm1Rps; ++q) {
+            float out[1] = {0.f};
+            if (!aborted && active && lo + spr * j + kQm1Rps * team + q < hi) {
+                Q3Slice<WPL> sl;
+                read_slice<WPL>(blk0 + (size_t)s * a.stage_bytes + (size_t)q * a.row_bytes, l0, sl);
+                dot_slice<1, WPL>(sl, lsel, hsel, xq, d8, c4, out);
+            }
+            v[q] = out[0];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const int c = atomicAdd(&released[s], 1);
+            // the warp that was last out of the previous stage refills its slot
+            if (prev_count == prev_last && prev_j >= 0 && prev_j + a.depth < nst && !*abort_flag)
+                issue(prev_j + a.depth, prev_s);
+            prev_count = c;
+        }
+        prev_j = j;
+        prev_s = s;
+        prev_last = kQm1Warps * (kd + 1) - 1;
+        if (++s == a.depth) {
+            s = 0;
+            parity ^= 1u;
+            ++kd;
+        }
+    };
+    constexpr int kSpg = kQm1Rows / kQm1Rps;  // stages per reduction
+    for (int j0 = 0; j0 < nst; j0 += kSpg) {
+        float v[kQm1Rows];
+#pragma unroll
+        for (int g = 0; g < kSpg; ++g) {
+            if (j0 + g < nst) {
+                stage(j0 + g, v + kQm1Rps * g);
+            } else {
+#pragma unroll
+                for (int q = 0; q < kQm1Rps; ++q)
+                    v[kQm1Rps * g + q] = 0.f;
+            }
+        }
+        // lanes 8k .. 8k+7 hold the warp's sum for value k: row q = k % Rps
+        // of the team in stage j0 + k / Rps
+        const int k = lane >> 3;
+        const int rl = spr * (j0 + k / kQm1Rps) + kQm1Rps * team + k % kQm1Rps;  // row within the CTA's range
+        const float r = reduce4_rows(v, lane);
+        if ((lane & 7) == 0 && lo + rl < hi)
+            red[(size_t)rl * a.wpt + wit] = r;
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // every copy issued must land before the CTA's shared memory goes away
+        // (the u-th copy into a slot completes the slot's phase u - 1)
+        if (tid < a.depth && uses[tid] > 0)
+            mbar_wait_bounded(smem_u32(&full_b[tid]), (uint32_t)(uses[tid] - 1) & 1u, nullptr);
+        if (tid == 0)
+            mbar_wait_bounded(smem_u32(xbar), 0, nullptr);
+        __syncthreads();
+        return;
+    }
+    // the team's warps (the chunks) of each row, added in order
+    for (int i = tid; i < hi - lo; i += blockDim.x) {
+        float v = 0.f;
+        for (int w = 0; w < a.wpt; ++w)
+            v += red[(size_t)i * a.wpt + w];
+        a.y[lo + i] = v;
+    }
+}
+
+// The launch plan of q3k_m1_kernel; false when the problem is not its: one
+// token on one matrix, rows of 16..128 blocks in 16-byte multiples (K a
+// multiple of 2048), W and x on 16-byte boundaries.
+bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, size_t& smem)
+{
+    if (p.m != 1 || p.W_table || p.n_seg != 1 || p.N < 1 || p.N > (int64_t(1) << 30))
+        return false;
+    if (p.K % 2048 || p.K < 16 * 256 || p.K > 128 * 256)
+        return false;
+    if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.x)) & 15u)
+        return false;
+    a = Qm1Args{};
+    a.nb = (int)(p.K / 256);
+    a.lanes = 32;
+    a.log_lanes = 5;
+    while (a.lanes < 2 * a.nb) {
+        a.lanes *= 2;
+        ++a.log_lanes;
+    }
+    a.teams = kQm1Threads / a.lanes;
+    a.wpt = a.lanes / 32;
+    a.row_bytes = (uint32_t)(a.nb * kQ3Bytes);
+    a.stage_bytes = (uint32_t)(kQm1Rps * a.teams) * a.row_bytes;
+    a.x_bytes = (uint32_t)(a.nb * 8 * kQ8Bytes);
+    a.W = static_cast<const uint8_t*>(p.W);
+    a.x = static_cast<const uint8_t*>(p.x);
+    a.y = p.y;
+    grid = (int)std::min<int64_t>(di.sm_count, p.N);
+    a.rows_q = (int)(p.N / grid);
+    a.rows_r = (int)(p.N % grid);
+    const size_t cap = std::min<size_t>((size_t)di.smem_optin, 227 * 1024);
+    const size_t red_bytes = (size_t)(a.rows_q + 1) * a.wpt * sizeof(float);
+    for (int depth = 8; depth >= 2; --depth) {
+        a.depth = depth;
+        a.off_x = (uint32_t)((size_t)depth * a.stage_bytes);
+        a.off_bar = a.off_x + (a.x_bytes + 15u) / 16u * 16u;
+        a.off_red = (uint32_t)(((size_t)a.off_bar + (size_t)(depth + 2) * sizeof(uint64_t) +
+                                (size_t)(2 * depth) * sizeof(int) + 15) / 16 * 16);
+        smem = ((size_t)a.off_red + red_bytes + 15) / 16 * 16;
+        if (smem <= cap)
+            return true;
+    }
+    return false;
+}
+
+cudaError_t launch_q3m1(const Qm1Args& a, int grid, size_t smem, cudaStream_t s)
+{
+    static std::atomic<unsigned long long> smem_devs{0};
+    cudaError_t e = allow_max_smem(q3k_m1_kernel, smem_devs);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(q3k_m1_kernel, dim3((unsigned)grid), dim3(kQm1Threads), smem, s, a);
+}
+
 }  // namespace
 
 cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
@@ -404,6 +689,13 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
         return e;
     if (q3mt_supported(p))  // several tokens: the tensor-core kernel
         return launch_q3k_mt(p, s);
+    {
+        Qm1Args a1;
+        int grid1;
+        size_t smem1;
+        if (plan_q3m1(p, di, a1, grid1, smem1))  // one token over long rows: row teams
+            return launch_q3m1(a1, grid1, smem1, s);
+    }
     const int nb = (int)(p.K / 256);
     // tokens per walk over the rows: one, or pairs (groups of four tokens
     // in 4-byte slices measured slower: 188 vs 103 us for m = 4 at 16384^2)

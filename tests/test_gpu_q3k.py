@@ -188,6 +188,34 @@ def test_q3k_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
     assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
 
 
+# one token over long rows (K a multiple of 2048 from 4096 to 32768, W and x
+# on 16-byte boundaries) runs the row-team kernel: teams of 32 to 256 lanes,
+# lanes past the row (K = 6144: 48 of 64), fewer rows than SMs, a row more on
+# some CTAs, many stages per CTA
+@pytest.mark.parametrize("N,K", [(1, 4096), (153, 6144), (300, 8192), (2000, 4096), (400, 32768)])
+def test_q3k_row_team_kernel_against_oracle(lib, N, K):
+    W = synth.q3k_matrix(12, f"q3.rt.{N}.{K}", N, K)
+    x = synth.bf16_normal(12, f"q3.rt.x.{K}", (1, K))
+    xq = oracle.q8_1_quantize(x)
+    y = lib.q3k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
+    assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, 1, K))) <= TOL_EXACT_X
+
+
+# the expert batches keep the general kernel; their rows still equal single
+# calls bit for bit where a single call takes the row-team kernel
+@pytest.mark.parametrize("K", [4096, 6144, 16384])
+@pytest.mark.parametrize("per_matrix", [False, True])
+def test_q3k_experts_equal_singles_on_row_team_shapes(lib, K, per_matrix):
+    n_mat, N = 3, 300
+    mats = [dev(synth.q3k_matrix(13, f"q3rt.{K}.{e}", N, K)) for e in range(n_mat)]
+    rows = n_mat if per_matrix else 1
+    xq = lib.q8_1_quantize_rows(bf16_dev(synth.bf16_normal(13, f"q3rt.x{rows}.{K}", (rows, K))))
+    y, _ = lib.q3k_mmvq_experts(lib.pointer_table(mats), N, K, xq, x_per_matrix=per_matrix)
+    for e in range(n_mat):
+        xe = xq[e:e + 1] if per_matrix else xq
+        assert torch.equal(y[e:e + 1], lib.q3k_mmvq_q8_1(mats[e], xe, K)), e
+
+
 def test_q3k_experts_moe_shapes_against_oracle(lib):
     # gate/up batch: 16 matrices [2048, 4096] over one row; down batch:
     # 8 matrices [4096, 2048], one row each (sampled output rows)
