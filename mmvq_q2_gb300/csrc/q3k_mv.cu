@@ -39,7 +39,8 @@
 //    through the 1.5*2^23 bias (one IMAD and one FADD, exact below 2^22),
 //    then meets the q8_1 scale in one FFMA.
 //  * Two tokens run as a group inside the launch; three to eight go to the
-//    tensor-core kernel of q3k_mt.cu (routed in launch_q3k_mv).
+//    tensor-core kernel of q3k_mt.cu, and one token over long rows to the
+//    row-team kernel below (q3k_m1_kernel), both routed in launch_q3k_mv.
 //  * A butterfly shuffle sum gives every lane the chunk's partial for a
 //    row, kept in shared memory; after one barrier the chunks are added in
 //    chunk order, so the result does not depend on scheduling.
