@@ -39,8 +39,9 @@
 //    through the 1.5*2^23 bias (one IMAD and one FADD, exact below 2^22),
 //    then meets the q8_1 scale in one FFMA.
 //  * Two tokens run as a group inside the launch; three to eight go to the
-//    tensor-core kernel of q3k_mt.cu, and one token over long rows to the
-//    row-team kernel below (q3k_m1_kernel), both routed in launch_q3k_mv.
+//    tensor-core kernel of q3k_mt.cu, and one or two tokens over long rows
+//    to the row-team kernel below (q3k_m1_kernel), both routed in
+//    launch_q3k_mv.
 //  * A butterfly shuffle sum gives every lane the chunk's partial for a
 //    row, kept in shared memory; after one barrier the chunks are added in
 //    chunk order, so the result does not depend on scheduling.
@@ -395,32 +396,36 @@ int q3_lw(int mg, int nb)
     return lw;
 }
 
-// ---- one token over long rows: row teams over a ring of whole rows ----
+// ---- one or two tokens over long rows: row teams over a ring of whole rows ----
 //
 // The design of the Q2_K one-token kernel (q2k_m1.cu) with Q3_K blocks.
 // One CTA of 16 warps per SM owns a contiguous range of rows.  A row team
-// has two lanes per block column, each with the 16-byte-position slice
-// (128 weights) that read_slice / dot_slice take, so every lane keeps its
-// q8_1 activations in registers for every row it visits.  Whole rows arrive
+// has two lanes per block column for one token (16-byte-position slices,
+// 128 weights) or four for two tokens (8-byte slices), the slices that
+// read_slice / dot_slice take, so every lane keeps its q8_1 activations in
+// registers for every row it visits.  Whole rows arrive
 // by 1-D bulk copies into a ring of stages (two rows per team a stage); the
 // warp last out of a stage refills its slot one stage later.  A lane's
 // partial, the warp's butterfly sum (xor 16, 8, 4, 2, 1) and the sum of the
-// team's warps in warp order are the same operations, in the same order,
-// as q3k_mv_kernel<1, 16> performs (its warp covers the same 16 block
-// columns), so both give the same bits: the expert batches, which run
-// there, keep equal to single calls.
+// team's warps in warp order are, for one token, the same operations, in
+// the same order, as q3k_mv_kernel<1, 16> performs (its warp covers the
+// same 16 block columns), so both give the same bits: the expert batches,
+// which run there, keep equal to single calls.
 constexpr int kQm1Threads = 512;
 constexpr int kQm1Warps = kQm1Threads / 32;
-constexpr int kQm1Lw = 16;   // byte positions per lane: 128 weights of a block
 constexpr int kQm1Rps = 2;   // rows per team in a stage
+// byte positions per lane: 16 (128 weights of a block) for one token, 8 for two
+__host__ __device__ constexpr int qm1_lw(int mg) { return mg == 1 ? 16 : 8; }
 constexpr int kQm1Rows = 4;  // rows per lane between two warp reductions (two stages)
 
 struct Qm1Args {
     const uint8_t* W;
     float* y;
-    const uint8_t* x;  // one q8_1 row
+    const uint8_t* x;  // q8_1 rows, one per token
+    int64_t x_tok_stride;  // bytes between tokens' rows (a multiple of 16)
+    int64_t ldy;           // floats between tokens of y
     int nb;
-    int lanes;         // lanes per row team: a power of two >= 2 * nb, 32..256
+    int lanes;         // lanes per row team: a power of two >= (32 / LW) * nb, 32..512
     int log_lanes;
     int teams;         // kQm1Threads / lanes
     int wpt;           // warps per team
@@ -430,29 +435,43 @@ struct Qm1Args {
     uint32_t off_x, off_bar, off_red;
 };
 
-// The warp sums of v[0..3]: lane L returns the sum of v[L >> 3] over the
-// warp, paired as a butterfly over lane bits 4, 3, 2, 1, 0.
-__device__ __forceinline__ float reduce4_rows(const float (&v)[4], int lane)
+// The warp sums of v[0..VP-1] (VP = 4 or 8): lane L returns the sum of
+// v[L / (32 / VP)] over the warp, paired as a butterfly over lane bits 4,
+// 3, 2, 1, 0.  The first log2(VP) steps halve the values a lane holds: it
+// keeps the half its lane bit selects and adds its partner's copy of it.
+template <int VP>
+__device__ __forceinline__ float reduce_rows(const float (&v)[VP], int lane)
 {
-    const bool up = (lane & 16) != 0;
-    float a0 = up ? v[2] : v[0], a1 = up ? v[3] : v[1];
-    const float b0 = up ? v[0] : v[2], b1 = up ? v[1] : v[3];
-    a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
-    a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
-    const bool u8 = (lane & 8) != 0;
-    float c = u8 ? a1 : a0;
-    const float e = u8 ? a0 : a1;
-    c += __shfl_xor_sync(0xffffffffu, e, 8);
-    c += __shfl_xor_sync(0xffffffffu, c, 4);
-    c += __shfl_xor_sync(0xffffffffu, c, 2);
-    c += __shfl_xor_sync(0xffffffffu, c, 1);
-    return c;
+    static_assert(VP == 4 || VP == 8, "four or eight values a lane");
+    float a[VP];
+#pragma unroll
+    for (int i = 0; i < VP; ++i)
+        a[i] = v[i];
+    int bit = 16;
+#pragma unroll
+    for (int n = VP; n > 1; n >>= 1, bit >>= 1) {
+        const bool up = (lane & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? a[n / 2 + i] : a[i];
+            const float send = up ? a[i] : a[n / 2 + i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+    }
+#pragma unroll
+    for (; bit >= 1; bit >>= 1)
+        a[0] += __shfl_xor_sync(0xffffffffu, a[0], bit);
+    return a[0];
 }
 
+template <int MG>
 __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int WPL = kQm1Lw / 4;
+    constexpr int LW = qm1_lw(MG);
+    constexpr int WPL = LW / 4;
+    constexpr int LPB = 32 / LW;            // lanes per block column
+    constexpr int VP = kQm1Rows * MG;       // values per lane between two reductions
     pdl_launch_dependents();  // the next kernel may set itself up meanwhile
 
     const int tid = threadIdx.x;
@@ -504,8 +523,11 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
     if (tid == 0) {
         // the activations first (every CTA reads them: keep them in L2), then
         // the whole ring
-        mbar_arrive_expect_tx(smem_u32(xbar), a.x_bytes);
-        bulk_copy_g2s_hint(smem_u32(smem + a.off_x), a.x, a.x_bytes, smem_u32(xbar), l2_policy_evict_last());
+        mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)MG * a.x_bytes);
+#pragma unroll
+        for (int t = 0; t < MG; ++t)
+            bulk_copy_g2s_hint(smem_u32(smem + a.off_x + (size_t)t * a.x_bytes), a.x + (int64_t)t * a.x_tok_stride,
+                               a.x_bytes, smem_u32(xbar), l2_policy_evict_last());
         for (int j = 0; j < min(a.depth, nst); ++j)
             issue(j, j);
     }
@@ -520,30 +542,33 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
         return false;
     };
 
-    // this lane's slice: block column b, byte positions l0 .. l0 + 15
-    const bool active = li < 2 * a.nb;
-    const int b = active ? li >> 1 : 0;
-    const int l0 = (li & 1) * kQm1Lw;
-    const uint32_t lsel = l0 ? 0x7531u : 0x6420u;
-    const uint32_t hsel = l0 ? 0x3131u : 0x2020u;
+    // this lane's slice: block column b, byte positions l0 .. l0 + LW - 1
+    const bool active = li < LPB * a.nb;
+    const int b = active ? li / LPB : 0;
+    const int l0 = (li % LPB) * LW;
+    const uint32_t lsel = (l0 >> 4) ? 0x7531u : 0x6420u;
+    const uint32_t hsel = (l0 >> 4) ? 0x3131u : 0x2020u;
     bool aborted = !wait(smem_u32(xbar), 0);
-    // q8_1 blocks 8b + 4n + j: d8, the lane's 16 q8 bytes, and the start of
-    // the (n, j) chain, -4 * 4^j * (their sum) (16 for j = 3)
-    uint32_t xq[1][8][WPL];
-    float d8[1][8];
-    int c4[1][8];
+    // per token, q8_1 blocks 8b + 4n + j: d8, the lane's q8 bytes, and the
+    // start of the (n, j) chain, -4 * 4^j * (their sum) (16 for j = 3)
+    uint32_t xq[MG][8][WPL];
+    float d8[MG][8];
+    int c4[MG][8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint8_t* xb = xsm + ((size_t)b * 8 + k) * kQ8Bytes;
-        d8[0][k] = active ? half_lo_f(lds32(xb)) : 0.f;
-        int sq = 0;
+    for (int t = 0; t < MG; ++t) {
 #pragma unroll
-        for (int w = 0; w < WPL; ++w) {
-            xq[0][k][w] = active ? lds32(xb + 4 + l0 + 4 * w) : 0u;
-            sq = dp4a_us(0x01010101u, xq[0][k][w], sq);
+        for (int k = 0; k < 8; ++k) {
+            const uint8_t* xb = xsm + (size_t)t * a.x_bytes + ((size_t)b * 8 + k) * kQ8Bytes;
+            d8[t][k] = active ? half_lo_f(lds32(xb)) : 0.f;
+            int sq = 0;
+#pragma unroll
+            for (int w = 0; w < WPL; ++w) {
+                xq[t][k][w] = active ? lds32(xb + 4 + l0 + 4 * w) : 0u;
+                sq = dp4a_us(0x01010101u, xq[t][k][w], sq);
+            }
+            const int j = k & 3;
+            c4[t][k] = -4 * sq * (j < 3 ? (1 << (2 * j)) : 16);
         }
-        const int j = k & 3;
-        c4[0][k] = -4 * sq * (j < 3 ? (1 << (2 * j)) : 16);
     }
 
     const uint8_t* blk0 = ring + (size_t)team * kQm1Rps * a.row_bytes + (size_t)b * kQ3Bytes;
@@ -558,13 +583,18 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
             aborted = true;
 #pragma unroll
         for (int q = 0; q < kQm1Rps; ++q) {
-            float out[1] = {0.f};
+            float out[MG];
+#pragma unroll
+            for (int t = 0; t < MG; ++t)
+                out[t] = 0.f;
             if (!aborted && active && lo + spr * j + kQm1Rps * team + q < hi) {
                 Q3Slice<WPL> sl;
                 read_slice<WPL>(blk0 + (size_t)s * a.stage_bytes + (size_t)q * a.row_bytes, l0, sl);
-                dot_slice<1, WPL>(sl, lsel, hsel, xq, d8, c4, out);
+                dot_slice<MG, WPL>(sl, lsel, hsel, xq, d8, c4, out);
             }
-            v[q] = out[0];
+#pragma unroll
+            for (int t = 0; t < MG; ++t)
+                v[q * MG + t] = out[t];
         }
         __syncwarp();
         if (lane == 0) {
@@ -585,25 +615,28 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
         }
     };
     constexpr int kSpg = kQm1Rows / kQm1Rps;  // stages per reduction
+    constexpr int kGl = 32 / VP;  // lanes that end with each value
     for (int j0 = 0; j0 < nst; j0 += kSpg) {
-        float v[kQm1Rows];
+        float v[VP];
 #pragma unroll
         for (int g = 0; g < kSpg; ++g) {
             if (j0 + g < nst) {
-                stage(j0 + g, v + kQm1Rps * g);
+                stage(j0 + g, v + kQm1Rps * MG * g);
             } else {
 #pragma unroll
-                for (int q = 0; q < kQm1Rps; ++q)
-                    v[kQm1Rps * g + q] = 0.f;
+                for (int q = 0; q < kQm1Rps * MG; ++q)
+                    v[kQm1Rps * MG * g + q] = 0.f;
             }
         }
-        // lanes 8k .. 8k+7 hold the warp's sum for value k: row q = k % Rps
-        // of the team in stage j0 + k / Rps
-        const int k = lane >> 3;
-        const int rl = spr * (j0 + k / kQm1Rps) + kQm1Rps * team + k % kQm1Rps;  // row within the CTA's range
-        const float r = reduce4_rows(v, lane);
-        if ((lane & 7) == 0 && lo + rl < hi)
-            red[(size_t)rl * a.wpt + wit] = r;
+        // lanes kGl*k .. kGl*k + kGl-1 hold the warp's sum for value k:
+        // token k % MG of row (k / MG) % Rps of the team in stage
+        // j0 + k / (Rps * MG)
+        const int k = lane / kGl;
+        const int kr = k / MG, t = k - kr * MG;
+        const int rl = spr * (j0 + kr / kQm1Rps) + kQm1Rps * team + kr % kQm1Rps;  // row within the CTA's range
+        const float r = reduce_rows<VP>(v, lane);
+        if ((lane & (kGl - 1)) == 0 && lo + rl < hi)
+            red[((size_t)rl * MG + t) * a.wpt + wit] = r;
     }
 
     __syncthreads();
@@ -617,34 +650,39 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
         __syncthreads();
         return;
     }
-    // the team's warps (the chunks) of each row, added in order
-    for (int i = tid; i < hi - lo; i += blockDim.x) {
+    // the team's warps (the chunks) of each (row, token), added in order
+    for (int i = tid; i < (hi - lo) * MG; i += blockDim.x) {
+        const int r = i / MG, t = i - r * MG;
         float v = 0.f;
         for (int w = 0; w < a.wpt; ++w)
             v += red[(size_t)i * a.wpt + w];
-        a.y[lo + i] = v;
+        a.y[(int64_t)t * a.ldy + lo + r] = v;
     }
 }
 
 // The launch plan of q3k_m1_kernel; false when the problem is not its: one
-// token on one matrix, rows of 16..128 blocks in 16-byte multiples (K a
-// multiple of 2048), W and x on 16-byte boundaries.
+// or two tokens on one matrix, rows of 16..128 blocks in 16-byte multiples
+// (K a multiple of 2048), W, x and the tokens' rows on 16-byte boundaries.
 bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, size_t& smem)
 {
-    if (p.m != 1 || p.W_table || p.n_seg != 1 || p.N < 1 || p.N > (int64_t(1) << 30))
+    if ((p.m != 1 && p.m != 2) || p.W_table || p.n_seg != 1 || p.N < 1 || p.N > (int64_t(1) << 30))
         return false;
     if (p.K % 2048 || p.K < 16 * 256 || p.K > 128 * 256)
         return false;
-    if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.x)) & 15u)
+    if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.x)) & 15u ||
+        (p.m > 1 && (p.x_tok_stride & 15)))
         return false;
     a = Qm1Args{};
     a.nb = (int)(p.K / 256);
+    const int lpb = 32 / qm1_lw(p.m);
     a.lanes = 32;
     a.log_lanes = 5;
-    while (a.lanes < 2 * a.nb) {
+    while (a.lanes < lpb * a.nb) {
         a.lanes *= 2;
         ++a.log_lanes;
     }
+    if (a.lanes > kQm1Threads)
+        return false;
     a.teams = kQm1Threads / a.lanes;
     a.wpt = a.lanes / 32;
     a.row_bytes = (uint32_t)(a.nb * kQ3Bytes);
@@ -652,16 +690,18 @@ bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, 
     a.x_bytes = (uint32_t)(a.nb * 8 * kQ8Bytes);
     a.W = static_cast<const uint8_t*>(p.W);
     a.x = static_cast<const uint8_t*>(p.x);
+    a.x_tok_stride = p.x_tok_stride;
     a.y = p.y;
+    a.ldy = p.ldy;
     grid = (int)std::min<int64_t>(di.sm_count, p.N);
     a.rows_q = (int)(p.N / grid);
     a.rows_r = (int)(p.N % grid);
     const size_t cap = std::min<size_t>((size_t)di.smem_optin, 227 * 1024);
-    const size_t red_bytes = (size_t)(a.rows_q + 1) * a.wpt * sizeof(float);
+    const size_t red_bytes = (size_t)(a.rows_q + 1) * p.m * a.wpt * sizeof(float);
     for (int depth = 8; depth >= 2; --depth) {
         a.depth = depth;
         a.off_x = (uint32_t)((size_t)depth * a.stage_bytes);
-        a.off_bar = a.off_x + (a.x_bytes + 15u) / 16u * 16u;
+        a.off_bar = a.off_x + (uint32_t)p.m * a.x_bytes;  // x_bytes is a multiple of 16
         a.off_red = (uint32_t)(((size_t)a.off_bar + (size_t)(depth + 2) * sizeof(uint64_t) +
                                 (size_t)(2 * depth) * sizeof(int) + 15) / 16 * 16);
         smem = ((size_t)a.off_red + red_bytes + 15) / 16 * 16;
@@ -671,13 +711,14 @@ bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, 
     return false;
 }
 
-cudaError_t launch_q3m1(const Qm1Args& a, int grid, size_t smem, cudaStream_t s)
+template <int MG>
+cudaError_t launch_q3m1_tpl(const Qm1Args& a, int grid, size_t smem, cudaStream_t s)
 {
     static std::atomic<unsigned long long> smem_devs{0};
-    cudaError_t e = allow_max_smem(q3k_m1_kernel, smem_devs);
+    cudaError_t e = allow_max_smem(q3k_m1_kernel<MG>, smem_devs);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(q3k_m1_kernel, dim3((unsigned)grid), dim3(kQm1Threads), smem, s, a);
+    return launch_pdl(q3k_m1_kernel<MG>, dim3((unsigned)grid), dim3(kQm1Threads), smem, s, a);
 }
 
 }  // namespace
@@ -694,8 +735,8 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
         Qm1Args a1;
         int grid1;
         size_t smem1;
-        if (plan_q3m1(p, di, a1, grid1, smem1))  // one token over long rows: row teams
-            return launch_q3m1(a1, grid1, smem1, s);
+        if (plan_q3m1(p, di, a1, grid1, smem1))  // one or two tokens over long rows: row teams
+            return p.m == 1 ? launch_q3m1_tpl<1>(a1, grid1, smem1, s) : launch_q3m1_tpl<2>(a1, grid1, smem1, s);
     }
     const int nb = (int)(p.K / 256);
     // tokens per walk over the rows: one, or pairs (groups of four tokens

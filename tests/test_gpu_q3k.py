@@ -188,17 +188,19 @@ def test_q3k_experts_rows_equal_singles_and_weighted_sum(lib, per_matrix):
     assert np.max(np.abs(ysum.cpu().numpy() - ref)) <= 1e-5 * np.linalg.norm(ref)
 
 
-# one token over long rows (K a multiple of 2048 from 4096 to 32768, W and x
-# on 16-byte boundaries) runs the row-team kernel: teams of 32 to 256 lanes,
-# lanes past the row (K = 6144: 48 of 64), fewer rows than SMs, a row more on
-# some CTAs, many stages per CTA
+# one or two tokens over long rows (K a multiple of 2048 from 4096 to 32768,
+# W and x on 16-byte boundaries) run the row-team kernel: teams of 32 to 512
+# lanes, lanes past the row (K = 6144: 48 of 64 for one token, 96 of 128 for
+# two), fewer rows than SMs, a row more on some CTAs, many stages per CTA
+@pytest.mark.parametrize("m", [1, 2])
 @pytest.mark.parametrize("N,K", [(1, 4096), (153, 6144), (300, 8192), (2000, 4096), (400, 32768)])
-def test_q3k_row_team_kernel_against_oracle(lib, N, K):
+def test_q3k_row_team_kernel_against_oracle(lib, N, K, m):
     W = synth.q3k_matrix(12, f"q3.rt.{N}.{K}", N, K)
-    x = synth.bf16_normal(12, f"q3.rt.x.{K}", (1, K))
+    x = synth.bf16_normal(12, f"q3.rt.x{m}.{K}", (m, K))
     xq = oracle.q8_1_quantize(x)
     y = lib.q3k_mmvq_q8_1(dev(W), dev(xq), K).cpu().numpy()
-    assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, 1, K))) <= TOL_EXACT_X
+    assert y.shape == (m, N)
+    assert rel_err_rows(y, oracle.q3k_matvec(W, N, K, oracle.q8_1_dequant(xq, m, K))) <= TOL_EXACT_X
 
 
 # the expert batches keep the general kernel; their rows still equal single
