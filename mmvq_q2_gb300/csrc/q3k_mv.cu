@@ -419,7 +419,10 @@ __host__ __device__ constexpr int qm1_lw(int mg) { return mg == 1 ? 16 : 8; }
 constexpr int kQm1Rows = 4;  // rows per lane between two warp reductions (two stages)
 
 struct Qm1Args {
-    const uint8_t* W;
+    const uint8_t* W;              // the matrix, or null with a table
+    const void* const* W_table;    // table: matrix e holds rows e*Nm .. e*Nm + Nm - 1 of the row space
+    int Nm;                        // rows per matrix of the table
+    int64_t y_seg_stride;          // floats between matrices' rows of y (table)
     float* y;
     const uint8_t* x;  // q8_1 rows, one per token
     int64_t x_tok_stride;  // bytes between tokens' rows (a multiple of 16)
@@ -464,9 +467,10 @@ __device__ __forceinline__ float reduce_rows(const float (&v)[VP], int lane)
     return a[0];
 }
 
-template <int MG>
+template <int MG, bool TAB>
 __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
 {
+    static_assert(!TAB || MG == 1, "expert tables: one token");
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int LW = qm1_lw(MG);
     constexpr int WPL = LW / 4;
@@ -520,6 +524,52 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
                            l2_policy_evict_first());
         atomicAdd(&uses[s], 1);
     };
+    // With a table, stage j into slot s by one whole warp: rows of a matrix
+    // on a 16-byte boundary arrive by bulk copy, rows of one on a 4-byte
+    // boundary are copied by the warp's lanes (words), rows of any other are
+    // not read (they are skipped at the end).  One arrival a stage, with the
+    // bulk bytes.
+    auto issue_tab = [&](int j, int s) {
+        const int r0 = lo + spr * j;
+        const int r1 = min(hi, r0 + spr);
+        uint8_t* dst0 = ring + (size_t)s * a.stage_bytes;
+        uint32_t tx = 0;
+        for (int r = r0; r < r1;) {
+            const int e = r / a.Nm;
+            const int re = min(r1, (e + 1) * a.Nm);
+            const uint8_t* wp = static_cast<const uint8_t*>(a.W_table[e]);
+            const uintptr_t u = reinterpret_cast<uintptr_t>(wp);
+            const uint32_t bytes = (uint32_t)(re - r) * a.row_bytes;
+            if ((u & 15u) == 0) {
+                tx += bytes;
+            } else if ((u & 3u) == 0) {
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(wp + (int64_t)(r - e * a.Nm) * a.row_bytes);
+                uint32_t* dst = reinterpret_cast<uint32_t*>(dst0 + (size_t)(r - r0) * a.row_bytes);
+                for (uint32_t w = (uint32_t)lane; w < bytes / 4u; w += 32u)
+                    dst[w] = __ldg(src + w);
+            }
+            r = re;
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t fb = smem_u32(&full_b[s]);
+            // the slot may hold words the lanes wrote: order them before the copies
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(fb, tx);
+            for (int r = r0; r < r1;) {
+                const int e = r / a.Nm;
+                const int re = min(r1, (e + 1) * a.Nm);
+                const uint8_t* wp = static_cast<const uint8_t*>(a.W_table[e]);
+                if ((reinterpret_cast<uintptr_t>(wp) & 15u) == 0)
+                    bulk_copy_g2s_hint(smem_u32(dst0 + (size_t)(r - r0) * a.row_bytes),
+                                       wp + (int64_t)(r - e * a.Nm) * a.row_bytes, (uint32_t)(re - r) * a.row_bytes,
+                                       fb, l2_policy_evict_first());
+                r = re;
+            }
+            atomicAdd(&uses[s], 1);
+        }
+    };
     if (tid == 0) {
         // the activations first (every CTA reads them: keep them in L2), then
         // the whole ring
@@ -528,8 +578,14 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
         for (int t = 0; t < MG; ++t)
             bulk_copy_g2s_hint(smem_u32(smem + a.off_x + (size_t)t * a.x_bytes), a.x + (int64_t)t * a.x_tok_stride,
                                a.x_bytes, smem_u32(xbar), l2_policy_evict_last());
-        for (int j = 0; j < min(a.depth, nst); ++j)
-            issue(j, j);
+        if constexpr (!TAB)
+            for (int j = 0; j < min(a.depth, nst); ++j)
+                issue(j, j);
+    }
+    if constexpr (TAB) {
+        if (tid < 32)
+            for (int j = 0; j < min(a.depth, nst); ++j)
+                issue_tab(j, j);
     }
     // every lane waits for itself; gives up after about two seconds
     auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -597,13 +653,26 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
                 v[q * MG + t] = out[t];
         }
         __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            const int c = atomicAdd(&released[s], 1);
-            // the warp that was last out of the previous stage refills its slot
-            if (prev_count == prev_last && prev_j >= 0 && prev_j + a.depth < nst && !*abort_flag)
-                issue(prev_j + a.depth, prev_s);
-            prev_count = c;
+        if constexpr (TAB) {
+            int refill = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                const int c = atomicAdd(&released[s], 1);
+                // the warp that was last out of the previous stage refills its slot
+                refill = prev_count == prev_last && prev_j >= 0 && prev_j + a.depth < nst && !*abort_flag;
+                prev_count = c;
+            }
+            if (__shfl_sync(0xffffffffu, refill, 0))
+                issue_tab(prev_j + a.depth, prev_s);
+        } else {
+            if (lane == 0) {
+                __threadfence_block();
+                const int c = atomicAdd(&released[s], 1);
+                // the warp that was last out of the previous stage refills its slot
+                if (prev_count == prev_last && prev_j >= 0 && prev_j + a.depth < nst && !*abort_flag)
+                    issue(prev_j + a.depth, prev_s);
+                prev_count = c;
+            }
         }
         prev_j = j;
         prev_s = s;
@@ -653,10 +722,22 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
     // the team's warps (the chunks) of each (row, token), added in order
     for (int i = tid; i < (hi - lo) * MG; i += blockDim.x) {
         const int r = i / MG, t = i - r * MG;
+        if constexpr (TAB) {
+            // a matrix off a 4-byte boundary was not read: its rows of y stay
+            if (reinterpret_cast<uintptr_t>(a.W_table[(lo + r) / a.Nm]) & 3u) {
+                atomicOr(&g_q3_error, 2);
+                continue;
+            }
+        }
         float v = 0.f;
         for (int w = 0; w < a.wpt; ++w)
             v += red[(size_t)i * a.wpt + w];
-        a.y[(int64_t)t * a.ldy + lo + r] = v;
+        if constexpr (TAB) {
+            const int e = (lo + r) / a.Nm;
+            a.y[(int64_t)e * a.y_seg_stride + (lo + r - e * a.Nm)] = v;
+        } else {
+            a.y[(int64_t)t * a.ldy + lo + r] = v;
+        }
     }
 }
 
@@ -665,11 +746,16 @@ __global__ void __launch_bounds__(kQm1Threads, 1) q3k_m1_kernel(const Qm1Args a)
 // (K a multiple of 2048), W, x and the tokens' rows on 16-byte boundaries.
 bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, size_t& smem)
 {
-    if ((p.m != 1 && p.m != 2) || p.W_table || p.n_seg != 1 || p.N < 1 || p.N > (int64_t(1) << 30))
+    // a table: one token, one input row shared by every matrix
+    const bool tab = p.W_table != nullptr;
+    const int64_t rows = tab ? p.N * p.n_seg : p.N;
+    if ((p.m != 1 && p.m != 2) || p.N < 1 || rows > (int64_t(1) << 30))
+        return false;
+    if (tab ? (p.m != 1 || p.x_seg_stride != 0 || p.n_seg < 1) : p.n_seg != 1)
         return false;
     if (p.K % 2048 || p.K < 16 * 256 || p.K > 128 * 256)
         return false;
-    if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.x)) & 15u ||
+    if (((tab ? 0u : reinterpret_cast<uintptr_t>(p.W)) | reinterpret_cast<uintptr_t>(p.x)) & 15u ||
         (p.m > 1 && (p.x_tok_stride & 15)))
         return false;
     a = Qm1Args{};
@@ -688,14 +774,17 @@ bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, 
     a.row_bytes = (uint32_t)(a.nb * kQ3Bytes);
     a.stage_bytes = (uint32_t)(kQm1Rps * a.teams) * a.row_bytes;
     a.x_bytes = (uint32_t)(a.nb * 8 * kQ8Bytes);
-    a.W = static_cast<const uint8_t*>(p.W);
+    a.W = tab ? nullptr : static_cast<const uint8_t*>(p.W);
+    a.W_table = p.W_table;
+    a.Nm = (int)p.N;
+    a.y_seg_stride = p.y_seg_stride;
     a.x = static_cast<const uint8_t*>(p.x);
     a.x_tok_stride = p.x_tok_stride;
     a.y = p.y;
     a.ldy = p.ldy;
-    grid = (int)std::min<int64_t>(di.sm_count, p.N);
-    a.rows_q = (int)(p.N / grid);
-    a.rows_r = (int)(p.N % grid);
+    grid = (int)std::min<int64_t>(di.sm_count, rows);
+    a.rows_q = (int)(rows / grid);
+    a.rows_r = (int)(rows % grid);
     const size_t cap = std::min<size_t>((size_t)di.smem_optin, 227 * 1024);
     const size_t red_bytes = (size_t)(a.rows_q + 1) * p.m * a.wpt * sizeof(float);
     for (int depth = 8; depth >= 2; --depth) {
@@ -711,14 +800,14 @@ bool plan_q3m1(const Q3Problem& p, const DeviceInfo& di, Qm1Args& a, int& grid, 
     return false;
 }
 
-template <int MG>
+template <int MG, bool TAB>
 cudaError_t launch_q3m1_tpl(const Qm1Args& a, int grid, size_t smem, cudaStream_t s)
 {
     static std::atomic<unsigned long long> smem_devs{0};
-    cudaError_t e = allow_max_smem(q3k_m1_kernel<MG>, smem_devs);
+    cudaError_t e = allow_max_smem(q3k_m1_kernel<MG, TAB>, smem_devs);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(q3k_m1_kernel<MG>, dim3((unsigned)grid), dim3(kQm1Threads), smem, s, a);
+    return launch_pdl(q3k_m1_kernel<MG, TAB>, dim3((unsigned)grid), dim3(kQm1Threads), smem, s, a);
 }
 
 }  // namespace
@@ -736,7 +825,9 @@ cudaError_t launch_q3k_mv(const Q3Problem& p, cudaStream_t s)
         int grid1;
         size_t smem1;
         if (plan_q3m1(p, di, a1, grid1, smem1))  // one or two tokens over long rows: row teams
-            return p.m == 1 ? launch_q3m1_tpl<1>(a1, grid1, smem1, s) : launch_q3m1_tpl<2>(a1, grid1, smem1, s);
+            return p.W_table ? launch_q3m1_tpl<1, true>(a1, grid1, smem1, s)
+                   : p.m == 1 ? launch_q3m1_tpl<1, false>(a1, grid1, smem1, s)
+                              : launch_q3m1_tpl<2, false>(a1, grid1, smem1, s);
     }
     const int nb = (int)(p.K / 256);
     // tokens per walk over the rows: one, or pairs (groups of four tokens

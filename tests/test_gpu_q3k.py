@@ -221,6 +221,29 @@ def test_q3k_experts_equal_singles_on_row_team_shapes(lib, K, per_matrix):
         assert torch.equal(y[e:e + 1], lib.q3k_mmvq_q8_1(mats[e], xe, K)), e
 
 
+def test_q3k_experts_row_team_table_entries_off_16_and_off_a_word(lib):
+    # a shared input over rows of 16 blocks takes the row-team kernel: the
+    # entry 4 bytes past a 16-byte boundary is copied by the lanes (word by
+    # word), the entry off a word is skipped and flagged; stages straddle
+    # the matrices (200 rows each, about 4 rows a CTA)
+    N, K = 200, 4096
+    mats = [synth.q3k_matrix(14, f"q3tab.{e}", N, K) for e in range(3)]
+    good = dev(mats[0])
+    buf4 = torch.zeros(mats[1].size + 16, dtype=torch.uint8, device="cuda")
+    buf4[4:4 + mats[1].size] = dev(mats[1].reshape(-1))
+    bad = torch.zeros(mats[2].size + 16, dtype=torch.uint8, device="cuda")
+    tbl = torch.tensor([good.data_ptr(), buf4.data_ptr() + 4, bad.data_ptr() + 2], dtype=torch.int64, device="cuda")
+    xq = dev(oracle.q8_1_quantize(synth.bf16_normal(14, "q3tab.x", (1, K))))
+    y = torch.full((3, N), 5.0, dtype=torch.float32, device="cuda")
+    lib.q2k_device_error(clear=True)
+    lib.q3k_mmvq_experts(tbl, N, K, xq, y=y)
+    torch.cuda.synchronize()
+    assert lib.q2k_device_error(clear=True) == 2
+    assert torch.equal(y[0:1], lib.q3k_mmvq_q8_1(good, xq, K))
+    assert torch.equal(y[1:2], lib.q3k_mmvq_q8_1(dev(mats[1]), xq, K))
+    assert (y[2] == 5.0).all()
+
+
 def test_q3k_experts_moe_shapes_against_oracle(lib):
     # gate/up batch: 16 matrices [2048, 4096] over one row; down batch:
     # 8 matrices [4096, 2048], one row each (sampled output rows)
