@@ -22,17 +22,20 @@
 //                tensor copies into shared memory, one stage per A slot;
 //   warp 1       allocates tensor memory and issues tcgen05.mma (M = 128,
 //                N = token tile, K = 16; A from tensor memory, B from shared
-//                memory) from one thread;
+//                memory): for token tiles up to 64 the whole warp walks the
+//                stages and one elected lane issues, wider tiles from one
+//                thread;
 //   warps 12-15  read a finished accumulator back (tcgen05.ld) and store or
 //                add it into y while the next one fills (two accumulators
 //                when the token tile is at most 128 wide).
 // Measured on this GPU, and the reasons for the shape:
 //   * the tensor work of a tcgen05.mma of M = 128, K = 16 is about N/2
 //     cycles (128 at N = 256), while one thread issuing alone spends about
-//     50 cycles per MMA: narrow token tiles gain little, so one token tile
-//     of up to 256 serves every token count up to 256, and the expansion
-//     goes to tensor memory (its stores do not compete with the MMA's
-//     operand reads in shared memory);
+//     50 cycles per MMA (about 20 with the whole warp walking the loop):
+//     narrow token tiles gain little, so one token tile of up to 256 serves
+//     every token count up to 256, and the expansion goes to tensor memory
+//     (its stores do not compete with the MMA's operand reads in shared
+//     memory);
 //   * the issuing thread's own mbarrier waits, commits and MMA issues cost
 //     about 100, 70 and 64 cycles each, even when nothing is pending.  So a
 //     stage is 128 K (8 MMAs) behind ONE barrier: "full" completes when the
@@ -89,6 +92,7 @@ struct MqArgs {
     int64_t units;    // (tile, raw stage) units of one token tile
     int ctas;         // CTAs sharing the units of one token tile
     int atomic;       // partial tiles add into y
+    int warp_issue;   // the instance whose MMA issuer's loop runs on its whole warp (token tiles up to 64)
     uint32_t b_box;   // bytes of one 64-K activation box: ntok x 128
     uint32_t off_raw, off_bar;
 };
@@ -174,6 +178,9 @@ struct UnitWalk {
     }
 };
 
+// WI: the MMA issuer's loop runs on its whole warp (token tiles up to 64);
+// otherwise on one thread.  Two instances, so each holds one issuer loop.
+template <bool WI>
 __global__ void __launch_bounds__(kMqThreads, 1)
     q2k_mmq_kernel(const MqArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tx)
 {
@@ -283,8 +290,64 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {  // MMA issuer: one wait and one commit per stage
+    } else if (WI && warp == 1) {
+        // MMA issuer for token tiles up to 128: the whole warp walks the
+        // stages (one wait and one commit per stage), one elected lane issues
+        const uint32_t idesc = instr_desc(a.ntok);
+        const uint32_t box16 = a.b_box >> 4;  // descriptor address units
+        bool ok = true;
+        int s = 0, pc = 0;
+        uint32_t ph = 0;
+        UnitWalk w(u0, a.nrs);
+        for (int i = 0; i < nu && ok; ++i, w.next(a.nrs)) {
+            const bool fresh = i == 0 || w.st == 0;  // first unit of a piece
+            const int buf = pc % a.nacc;
+            if (fresh && pc >= a.nacc &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&acc_empty[buf]), (uint32_t)(pc / a.nacc - 1) & 1u,
+                                                           abort_flag))) {
+                ok = false;
+                break;
+            }
+            const uint32_t dt = tmem + (uint32_t)buf * a.acc_stride;
+            for (int k8 = 0; k8 < kMqStages; ++k8) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t at = tmem + a.a_col0 + (uint32_t)s * kACols;
+                const uint64_t bd = smem_desc_sw128(smem_u32(bring + (size_t)s * b_bytes));
+#pragma unroll
+                for (int k = 0; k < kSK / 16; ++k) {  // K = 16 per MMA: 8 A columns; 32 bytes along B's row
+                    if (elect_one())
+                        umma_f16_tmem_a(dt, at + 8 * k, bd + (uint64_t)((k >> 2) * box16 + 2 * (k & 3)), idesc,
+                                        !(fresh && k8 == 0 && k == 0));
+                }
+                if (elect_one())
+                    umma_commit(smem_u32(&empty[s]));  // the slot and the stage are free once these MMAs are done
+                __syncwarp();
+                if (++s == a.nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok && (i + 1 == nu || w.st + 1 == a.nrs)) {
+                if (elect_one())
+                    umma_commit(smem_u32(&acc_full[buf]));  // this accumulator is complete
+                __syncwarp();
+                ++pc;
+            }
+        }
+        if (!ok && lane == 0)
+            give_up();
+        // every MMA issued so far has finished once this arrives
+        if (elect_one())
+            umma_commit(smem_u32(mma_done));
+        __syncwarp();
+        mbar_wait_bounded(smem_u32(mma_done), 0u, nullptr);
+        __syncwarp();
+    } else if (!WI && warp == 1) {
+        if (lane == 0) {  // MMA issuer (wider tiles): one thread, one wait and one commit per stage
             const uint32_t idesc = instr_desc(a.ntok);
             const uint32_t box16 = a.b_box >> 4;  // descriptor address units
             bool ok = true;
@@ -494,6 +557,9 @@ bool plan_mmq(int64_t m, int64_t N, int64_t K, const DeviceInfo& di, MqPlan& p)
     a.N = (int)N;
     a.ntok = (int)std::min<int64_t>(256, (m + 15) / 16 * 16);
     a.nacc = a.ntok <= 128 ? 2 : 1;
+    // whole-warp issue: 63.1 / 65.4 us at m = 16 / 64 (16384^2) against
+    // 67.1 / 69.0 from one thread; mixed at 128-wide tiles, slower at 256
+    a.warp_issue = a.ntok <= 64 ? 1 : 0;
     a.acc_stride = 128;
     a.a_col0 = 256;
     a.b_box = (uint32_t)a.ntok * kBK * 2;
@@ -578,15 +644,16 @@ cudaError_t launch_mmq_bf16(const void* W, int64_t N, int64_t K, const uint16_t*
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    static std::atomic<unsigned long long> smem_devs{0};
-    if ((e = allow_max_smem(q2k_mmq_kernel, smem_devs)) != cudaSuccess)
+    auto kern = a.warp_issue ? q2k_mmq_kernel<true> : q2k_mmq_kernel<false>;
+    static std::atomic<unsigned long long> smem_devs[2] = {{0}, {0}};
+    if ((e = allow_max_smem(kern, smem_devs[a.warp_issue ? 1 : 0])) != cudaSuccess)
         return e;
     if (a.atomic) {
         e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), (size_t)m, s);
         if (e != cudaSuccess)
             return e;
     }
-    return launch_pdl(q2k_mmq_kernel, p.grid, dim3(kMqThreads), p.smem, s, a, tq, tx);
+    return launch_pdl(kern, p.grid, dim3(kMqThreads), p.smem, s, a, tq, tx);
 }
 
 cudaError_t launch_q8_1_to_bf16(const void* xq, int64_t m, int64_t K, uint16_t* out, cudaStream_t s)
